@@ -1,0 +1,371 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused MoE expert forward on GB300.
+
+One step = the whole hot path on one batch: top-k routing of the router
+logits, then the fused expert forward (schedule tables + gather, L1 grouped
+GEMM + SwiGLU/requant epilogue, L2 grouped GEMM, combine), all in this
+repository's CUDA kernels through the C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line.  N > 1 runs under torchrun as independent replicas
+(the path has no data exchange on one GPU), barrier + max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_expert_ffn_route_gb300 import synth  # noqa: E402
+
+METRIC = "fused MoE fwd tokens/s & TFLOP/s, % of roofline (1×GB300)"
+DEFAULT_WORKLOAD = "medium"
+L2_BYTES = 129 * 1024 * 1024
+KERNELS_PER_STEP = 6      # route, layout count, dispatch/gather, L1 GEMM, L2 GEMM, combine
+
+
+def peaks():
+    """Measured HBM GB/s and FP8-rate (block-scaled mxf8f6f4) TFLOP/s."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        m = json.load(open(path))
+        # the block-scaled FP8xFP4 MMA runs at the FP8 rate: 2x bf16 (nominal 4.5 / 2.25)
+        return dict(hbm_gbs=m["hbm_gbs"], fp8_tflops=2.0 * m["bf16_tflops"],
+                    fp8_tflops_sustained=2.0 * m["bf16_tflops_sustained"], source="measured")
+    return dict(hbm_gbs=6800.0, fp8_tflops=3800.0, fp8_tflops_sustained=3400.0, source="fallback")
+
+
+def algorithmic(wl, counts):
+    """Useful FLOPs and algorithmic HBM bytes of one forward (and of the L1
+    GEMM launch alone), counting only experts that receive rows."""
+    N = wl.N
+    H, I = wl.H, wl.I
+    touched = int((counts > 0).sum())
+    f_l1 = 2.0 * N * 2 * H * I
+    f_l2 = 2.0 * N * H * I
+    w1 = touched * 2 * I * H * (0.5 + 1 / 32)          # E2M1 + UE8M0
+    w2 = touched * H * I * (0.5 + 1 / 32)
+    act_x = N * H * (1 + 1 / 32)                        # gathered E4M3 rows + scales
+    act_h = N * I * (1 + 1 / 32)
+    y_pool = 2.0 * N * H
+    b_l1 = w1 + act_x + act_h                           # reads W1 and X, writes H
+    b_l2 = w2 + act_h + y_pool                          # reads W2 and H, writes Y rows
+    total_b = w1 + w2 + act_x + 2 * act_h + y_pool      # the pages' byte model plus scales
+    return dict(flops=f_l1 + f_l2, bytes=total_b, l1_flops=f_l1, l1_bytes=b_l1,
+                l2_flops=f_l2, l2_bytes=b_l2, touched=touched)
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_from_profile(kernel_src_hash: str, workload: str, units_scale: float):
+    """DRAM bytes per L1 GEMM launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "l1_gemm_traffic.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"kernel source sha256:\s*([0-9a-f]{16,64})", text)
+    m_val = re.search(rf"dram bytes per launch \({workload}\):\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_val or not kernel_src_hash.startswith(m_hash.group(1)):
+        return None
+    return float(m_val.group(1)) * units_scale
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm_kernels.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "moe_expert_ffn_route_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def cpu_baseline(wl, inp, idx, w, budget_s: float = 10.0):
+    """The oracle as it stands on this host's cores, on a bounded token sample."""
+    import oracle
+    rng = np.random.default_rng(0)
+    n = min(8, wl.T)
+    t0 = time.perf_counter()
+    oracle.forward(inp, idx, w, tokens=rng.choice(wl.T, n, replace=False))
+    dt = time.perf_counter() - t0
+    n2 = int(min(wl.T, max(n, n * budget_s / max(dt, 1e-3))))
+    toks = rng.choice(wl.T, n2, replace=False)
+    t0 = time.perf_counter()
+    oracle.forward(inp, idx, w, tokens=toks)
+    dt = time.perf_counter() - t0
+    return {"value": n2 / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n2} of {wl.T} tokens of workload {wl.name}, all k slots, fp64 direct loop"}
+
+
+def setup_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, wl):
+    """--impl reference: the oracle, timed on this host's cores (rank 0 only)."""
+    world, rank, _ = setup_dist()
+    if rank != 0:
+        return
+    import oracle
+    inp = synth.make_inputs(wl)
+    idx, w = oracle.route(inp["logits"], wl.k)
+    rng = np.random.default_rng(1)
+    n = min(wl.T, 8)
+    t0 = time.perf_counter()
+    oracle.forward(inp, idx, w, tokens=rng.choice(wl.T, n, replace=False))
+    per_tok = (time.perf_counter() - t0) / n
+    # each step: a token sample sized so that warmup + steps take about two minutes
+    n_step = int(max(1, min(wl.T, 120.0 / max(args.steps + args.warmup, 1) / max(per_tok, 1e-6))))
+    for _ in range(args.warmup):
+        oracle.forward(inp, idx, w, tokens=rng.choice(wl.T, n_step, replace=False))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward(inp, idx, w, tokens=rng.choice(wl.T, n_step, replace=False))
+    dt = time.perf_counter() - t0
+    value = n_step * args.steps / dt
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy generator)",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                       "tokens_per_step": n_step},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{n_step} random tokens of {wl.T} per step, all k slots"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    import torch
+    from moe_expert_ffn_route_gb300 import binding as mb
+
+    world, rank, local = setup_dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    inp = synth.make_inputs(wl)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    prob = mb.problem(T, H, I, E, k)
+    tile_n = mb.tile_n(prob)
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint32:
+            a = a.view(np.int32)
+        return torch.from_numpy(a).to(dev)
+
+    prepared = mb.prepare_weights(prob, up(inp["w1"]), up(inp["w1_sf"]), up(inp["w2"]), up(inp["w2_sf"]))
+    logits, x, x_sf = up(inp["logits"]), up(inp["x"]), up(inp["x_sf"])
+    idx = torch.empty((T, k), dtype=torch.int64, device=dev)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+    ws = mb.empty_workspace(prob, dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        mb.route_topk(logits, k, idx, wts)
+        if events is None:
+            mb.forward(prob, x, x_sf, idx, wts, prepared, ws, y)
+        else:
+            mb.forward_profiled(prob, x, x_sf, idx, wts, prepared, ws, y, events)
+
+    for _ in range(args.warmup):
+        step()
+        flush.fill_(1)
+    torch.cuda.synchronize()
+    st, code, _ = mb.device_status(prob, ws)
+    if st != mb.OK:
+        raise SystemExit(f"device status {mb.STATUS[st]} ({code})")
+    counts = mb.query(prob, ws, "counts").view(torch.int32)[:E].cpu().numpy()
+    alg = algorithmic(wl, counts)
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    stages = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        wall0 = time.perf_counter()
+        for i in range(K):
+            starts[i].record(stream)
+            step(stages[i])
+            ends[i].record(stream)
+            flush.fill_(i & 0xFF)         # L2 flush between steps, outside the timed intervals
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    stage_ms = np.array([[ev[j].elapsed_time(ev[j + 1]) for j in range(4)] for ev in stages])
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        torch.distributed.barrier()
+    ms_per_step = total_ms / K
+    tokens = T * K * world
+    value = tokens / (total_ms / 1e3)
+
+    # e2e through host buffers: pinned inputs -> device, route + forward, y -> pinned host
+    h_logits = torch.from_numpy(inp["logits"]).pin_memory()
+    h_x = torch.from_numpy(inp["x"]).pin_memory()
+    h_xsf = torch.from_numpy(inp["x_sf"].view(np.int32)).pin_memory()
+    h_y = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    h2d = h_logits.numel() * 4 + h_x.numel() + h_xsf.numel() * 4
+    d2h = T * H * 2
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for i in range(K):
+        e_s.record(stream)
+        logits.copy_(h_logits, non_blocking=True)
+        x.copy_(h_x, non_blocking=True)
+        x_sf.copy_(h_xsf, non_blocking=True)
+        step()
+        h_y.copy_(y, non_blocking=True)
+        e_e.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms += e_s.elapsed_time(e_e)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    pk = peaks()
+    l1_ms = float(stage_ms[:, 1].mean())
+    l2_ms = float(stage_ms[:, 2].mean())
+    compute_bound = alg["l1_flops"] / (pk["fp8_tflops"] * 1e12) >= alg["l1_bytes"] / (pk["hbm_gbs"] * 1e9)
+    if compute_bound:
+        achieved = alg["l1_flops"] / (l1_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["fp8_tflops"], "unit": "TFLOP/s"}
+    else:
+        achieved = alg["l1_bytes"] / (l1_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic_from_profile(kernel_hash(), wl.name, 1.0)
+    roof["kernel"] = "grouped_gemm_kernel<1> (L1 GEMM + SwiGLU/requant epilogue)"
+    roof["peak_source"] = (f"{pk['source']}: MEASURED_PEAKS bf16 burst x2 (FP8-rate block-scaled MMA)"
+                           if compute_bound else f"{pk['source']}: MEASURED_PEAKS hbm_gbs")
+    t_roof = max(alg["flops"] / (pk["fp8_tflops"] * 1e12), alg["bytes"] / (pk["hbm_gbs"] * 1e9))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxf8f6f4 (e4m3 x e2m1, ue8m0/32, fp32 accum, bf16 out)",
+        "data": "synthetic (seeded numpy generator; random-init expert weights)",
+        "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k, "tile_n": tile_n,
+                   "l2": "flushed between steps (256 MiB write outside the timed intervals)",
+                   "touched_experts": alg["touched"]},
+        "tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12 * world,
+        "hbm_gbs": alg["bytes"] / (ms_per_step / 1e3) / 1e9,
+        "roofline_step_frac": t_roof / (ms_per_step / 1e3),
+        "stage_ms": {"tables+gather": float(stage_ms[:, 0].mean()), "l1_gemm": l1_ms, "l2_gemm": l2_ms,
+                     "combine": float(stage_ms[:, 3].mean())},
+        "roofline": roof,
+        "e2e": {"value": T * K * world / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": KERNELS_PER_STEP * K,
+        "wall_s": wall,
+    }
+    line["clocks"] = clocks.summary()
+    if not args.no_cpu_baseline and world == 1:
+        import oracle
+        ridx, rw = oracle.route(inp["logits"], k)
+        line["cpu_baseline"] = cpu_baseline(wl, inp, ridx, rw)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

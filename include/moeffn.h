@@ -1,0 +1,226 @@
+/*
+ * moeffn.h -- C ABI of the fused MoE expert forward for one GB300 (sm_103a).
+ *
+ * The calls follow the problem statement of DeepGEMM's MegaMoE as the pages
+ * describe it (MegaMoE code-reading notes, "Host wrapper: how to call
+ * MegaMoE" and "Out-of-kernel preparation"): FP8 E4M3 tokens x with packed
+ * UE8M0 scales x_sf, topk_idx, topk_weights, and two expert weight sets in
+ * FP4 E2M1 with packed UE8M0 scales, producing BF16 y.  The one-GPU path is:
+ *
+ *   moeffn_route_topk      top-k routing from router logits
+ *   moeffn_forward         per-expert count -> 128-row padded prefix ->
+ *                          (token, k) -> slot table -> gather into the
+ *                          expert-sorted pool -> L1 grouped GEMM (E4M3 x E2M1,
+ *                          UE8M0 per 32) + SwiGLU x top-k weight + amax ->
+ *                          UE8M0 -> E4M3 -> L2 grouped GEMM -> BF16 ->
+ *                          top-k combine back to token order
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller (e.g. from
+ *    PyTorch); the library allocates and frees nothing.  Host-only calls are
+ *    marked as such.
+ *  - Row-major, densely packed; element type and shape in each comment.
+ *  - E2M1 packing: two codes per byte, element 2i in the low nibble.
+ *  - UE8M0 packing: four codes per uint32 along K; byte b (little-endian) of
+ *    word w covers K range [128w + 32b, 128w + 32b + 32).  One scale per row
+ *    per 32 consecutive K elements (recipe (1, 1, 32)).
+ *  - Calls that take a stream are asynchronous on it; a NULL stream is the
+ *    legacy default stream.  One workspace serves one forward in flight.
+ *  - Argument errors are reported synchronously, before anything is
+ *    launched.  Launch failures return MOEFFN_ERR_CUDA.  Data-dependent
+ *    errors found on the device (an expert id outside [-1, E), a bounded
+ *    wait that ran out) are recorded in the workspace's status word and read
+ *    with moeffn_get_device_status.
+ */
+#ifndef MOEFFN_H
+#define MOEFFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOEFFN_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MOEFFN_API __attribute__((visibility("default")))
+#else
+#define MOEFFN_API
+#endif
+
+typedef enum moeffn_status {
+    MOEFFN_OK = 0,
+    MOEFFN_ERR_INVALID_ARG = 1,          /* bad shape, null pointer, bad enum */
+    MOEFFN_ERR_UNSUPPORTED = 2,          /* not an sm_103 device, or an option not built */
+    MOEFFN_ERR_WORKSPACE_TOO_SMALL = 3,  /* a caller buffer is smaller than required */
+    MOEFFN_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
+    MOEFFN_ERR_TIMEOUT = 5               /* a bounded device wait ran out (device status) */
+} moeffn_status;
+
+/* A cudaStream_t / CUstream handle passed through untouched. */
+typedef void* moeffn_stream;
+
+/* Problem description.  Limits checked by every call that takes it:
+ *   num_tokens T >= 0; hidden H and intermediate I multiples of 128 (the
+ *   UE8M0 packing granularity, as the MegaMoE host checks require);
+ *   1 <= num_experts E <= 1024; 1 <= topk k <= min(E, 32).
+ * act_clamp: optional activation clamp of the L1 epilogue (MegaMoE notes,
+ *   "Activation clamp"); <= 0 disables it.  Values > 0 are not built yet and
+ *   return MOEFFN_ERR_UNSUPPORTED.
+ * fast_math: 0 = expf and IEEE division in SiLU.  Non-zero is not built yet
+ *   and returns MOEFFN_ERR_UNSUPPORTED.
+ * tile_n: token rows per grouped-GEMM tile: 0 = chosen from T*k/E, or one of
+ *   32, 64, 96, 128.
+ * wait_timeout_us: limit of every bounded device wait in microseconds;
+ *   0 = 2 000 000 (2 s).
+ * debug_flags: 0 for normal use.  Test hooks:
+ *   bit 0 (MOEFFN_DEBUG_STARVE_L1): the L1 GEMM's load warp skips its first
+ *     load, so the MMA warp's bounded wait runs out and the forward reports
+ *     MOEFFN_ERR_TIMEOUT through the device status instead of hanging;
+ *   bit 1 (MOEFFN_DEBUG_DUMP_L1_ACC): the forward stops after the L1 GEMM
+ *     and leaves its raw FP32 accumulators in the output-pool view as
+ *     float [P_max][2I] (gate channels 0..I-1, then up channels); needs
+ *     4*I <= H, else MOEFFN_ERR_UNSUPPORTED; y is not written.
+ * Pointers: x and y 16-byte aligned; prepared and workspace 256-byte
+ * aligned; other arrays aligned to their element size (INVALID_ARG). */
+typedef struct moeffn_problem {
+    int32_t num_tokens;
+    int32_t hidden;
+    int32_t intermediate;
+    int32_t num_experts;
+    int32_t topk;
+    float act_clamp;
+    int32_t fast_math;
+    int32_t tile_n;
+    int32_t wait_timeout_us;
+    int32_t debug_flags;
+} moeffn_problem;
+
+#define MOEFFN_DEBUG_STARVE_L1 1
+#define MOEFFN_DEBUG_DUMP_L1_ACC 2
+
+/* Views into a workspace after moeffn_forward (for inspection and tests).
+ * P_max = align(T*min(k,E) + E*127, 128) pool rows; P = offsets[E] <= P_max
+ * rows are in use; NT_max = ceil(T*k/32) + E token tiles.  Pool scale
+ * factors are stored per token tile (tile index tiles[e] + n for the n-th
+ * tile of expert e, covering pool rows offsets[e] + n*tile_n ...) and per
+ * 128-wide K block as 128 uint32 words; word 4*l + c holds the packed scales
+ * of tile row 32*c + l. */
+typedef enum moeffn_view {
+    MOEFFN_VIEW_STATUS = 0,     /* uint32 [16]: [0] error bits, [1] detail */
+    MOEFFN_VIEW_COUNTS = 1,     /* int32 [E]: rows routed to each expert */
+    MOEFFN_VIEW_OFFSETS = 2,    /* int32 [E+1]: first pool row of each expert, 128-row padded */
+    MOEFFN_VIEW_TILES = 3,      /* int32 [E+1]: first token tile of each expert */
+    MOEFFN_VIEW_SLOTS = 4,      /* int32 [T*k]: pool row of (t, j), -1 for an empty entry */
+    MOEFFN_VIEW_ROW2TK = 5,     /* int32 [P_max]: t*k+j of a pool row, -1 for padding */
+    MOEFFN_VIEW_WPOOL = 6,      /* float [P_max]: top-k weight of a pool row */
+    MOEFFN_VIEW_SLACK = 7,      /* int32 [P_max/128]: padding rows per 128-row block */
+    MOEFFN_VIEW_XPOOL = 8,      /* uint8 E4M3 [P_max][H]: gathered tokens */
+    MOEFFN_VIEW_XPOOL_SF = 9,   /* uint32 [NT_max][H/128][128]: their scales (tile layout) */
+    MOEFFN_VIEW_HPOOL = 10,     /* uint8 E4M3 [P_max][I]: requantised L1 output */
+    MOEFFN_VIEW_HPOOL_SF = 11,  /* uint32 [NT_max][I/128][128]: its scales (tile layout) */
+    MOEFFN_VIEW_YPOOL = 12      /* uint16 BF16 [P_max][H]: L2 output per pool row */
+} moeffn_view;
+
+/* Human-readable name of a status code (host only; never NULL). */
+MOEFFN_API const char* moeffn_status_string(moeffn_status status);
+
+/* MOEFFN_ABI_VERSION of the loaded library (host only). */
+MOEFFN_API int32_t moeffn_abi_version(void);
+
+/* Validate a problem description against the limits above (host only). */
+MOEFFN_API moeffn_status moeffn_check_problem(const moeffn_problem* problem);
+
+/* Token tile rows the forward will use for this problem (host only). */
+MOEFFN_API moeffn_status moeffn_tile_n(const moeffn_problem* problem, int32_t* tile_n);
+
+/* Bytes of device workspace moeffn_forward needs (host only).  It holds the
+ * schedule tables, the expert-sorted L1/L2 pools and their scales, and the
+ * L2 output pool; its contents need no initialisation. */
+MOEFFN_API moeffn_status moeffn_workspace_bytes(const moeffn_problem* problem, size_t* bytes);
+
+/* Bytes of device memory for the prepared weights (host only). */
+MOEFFN_API moeffn_status moeffn_prepared_weight_bytes(const moeffn_problem* problem, size_t* bytes);
+
+/* Re-lay the expert weights for the grouped GEMMs (MegaMoE blog 7.3 "L1
+ * weight interleave" and the SymmBuffer page's "transform_weights_for_mega_moe"
+ * section: gate/up interleave and scale transpose for tensor-memory copy).
+ *   w1     uint8 E2M1 [E][2I][H/2]  rows gate/up interleaved by 8
+ *                                   (gate 0..7, up 0..7, gate 8..15, ...)
+ *   w1_sf  uint32 UE8M0 [E][2I][H/128]
+ *   w2     uint8 E2M1 [E][H][I/2]
+ *   w2_sf  uint32 UE8M0 [E][H][I/128]
+ *   prepared       device buffer of moeffn_prepared_weight_bytes bytes,
+ *                  written by this call; opaque layout; must stay allocated
+ *                  and unmodified while forwards use it.
+ * Errors: null pointer -> INVALID_ARG; prepared_bytes too small ->
+ * WORKSPACE_TOO_SMALL; not sm_103 -> UNSUPPORTED. */
+MOEFFN_API moeffn_status moeffn_prepare_weights(const moeffn_problem* problem,
+                                     const uint8_t* w1, const uint32_t* w1_sf,
+                                     const uint8_t* w2, const uint32_t* w2_sf,
+                                     void* prepared, size_t prepared_bytes,
+                                     moeffn_stream stream);
+
+/* Top-k routing (MegaMoE notes "Problem background": the router picks the
+ * top-k experts of each token; the configs define it as softmax over the
+ * router logits, top-k, weights renormalised over the selected experts).
+ *   logits      float [T][E]; must not contain NaN; -inf allowed
+ *   topk_idx    int64 [T][k] out: experts by descending logit, ties to the
+ *               lower expert index
+ *   topk_w      float [T][k] out: exp(l_j - l_1) / sum_selected exp(l - l_1)
+ * Errors: E > 1024, k > min(E, 32), null pointers -> INVALID_ARG. */
+MOEFFN_API moeffn_status moeffn_route_topk(const float* logits, int32_t num_tokens, int32_t num_experts,
+                                int32_t topk, int64_t* topk_idx, float* topk_w,
+                                moeffn_stream stream);
+
+/* The fused expert forward (MegaMoE notes "Execution overview", steps 2-9,
+ * with the NVLink pull/push replaced by a local gather/scatter):
+ *   x          uint8 E4M3 [T][H]
+ *   x_sf       uint32 UE8M0 [T][H/128]
+ *   topk_idx   int64 [T][k]; -1 marks an empty entry (skipped); other values
+ *              outside [0, E) set a device error and are treated as -1
+ *   topk_w     float [T][k]; applied in the L1 epilogue (h = silu(g) * u * w)
+ *   prepared   output of moeffn_prepare_weights for this problem
+ *   workspace  device buffer of moeffn_workspace_bytes bytes
+ *   y          uint16 BF16 [T][H] out: sum over valid j of the BF16 L2 rows,
+ *              accumulated in FP32 in j order, rounded to BF16 (RNE)
+ * Errors: see the conventions above; workspace_bytes too small ->
+ * WORKSPACE_TOO_SMALL.  T = 0 launches nothing. */
+MOEFFN_API moeffn_status moeffn_forward(const moeffn_problem* problem,
+                             const uint8_t* x, const uint32_t* x_sf,
+                             const int64_t* topk_idx, const float* topk_w,
+                             const void* prepared, void* workspace, size_t workspace_bytes,
+                             uint16_t* y, moeffn_stream stream);
+
+/* moeffn_forward, additionally recording five caller-created CUDA events
+ * (cudaEvent_t handles, same device) on `stream` at the stage boundaries:
+ *   stage_events[0] before the schedule tables, [1] after the gather,
+ *   [2] after the L1 GEMM, [3] after the L2 GEMM, [4] after the combine.
+ * Lets a caller time each stage with cudaEventElapsedTime.  A NULL array
+ * or handle -> INVALID_ARG; otherwise errors as moeffn_forward. */
+MOEFFN_API moeffn_status moeffn_forward_profiled(const moeffn_problem* problem,
+                                                 const uint8_t* x, const uint32_t* x_sf,
+                                                 const int64_t* topk_idx, const float* topk_w,
+                                                 const void* prepared, void* workspace,
+                                                 size_t workspace_bytes, uint16_t* y,
+                                                 moeffn_stream stream, void* const* stage_events);
+
+/* Device pointer and byte size of one view of a workspace (host only; no
+ * GPU access).  Unknown view -> INVALID_ARG. */
+MOEFFN_API moeffn_status moeffn_query(const moeffn_problem* problem, void* workspace, int32_t view,
+                           void** dev_ptr, size_t* bytes);
+
+/* Synchronise `stream`, then read the workspace status word written by the
+ * last forward on it.  Returns MOEFFN_OK, MOEFFN_ERR_INVALID_ARG (an expert
+ * id outside [-1, E) was seen) or MOEFFN_ERR_TIMEOUT (a bounded wait ran
+ * out); *detail (optional) receives the raw status words [0] and [1]. */
+MOEFFN_API moeffn_status moeffn_get_device_status(const moeffn_problem* problem, void* workspace,
+                                       moeffn_stream stream, uint32_t* detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEFFN_H */

@@ -1,0 +1,75 @@
+// Internal launch interface between the C-ABI host code and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moeffn {
+
+struct DevStatus;
+
+struct LayoutArgs {
+    const uint8_t* x;
+    const uint32_t* x_sf;
+    const int64_t* topk_idx;
+    const float* topk_w;
+    int T, H, E, k, tile_n;
+    int* hist;      // [ceil(T*k/1024)][E]
+    int* rank;      // [T*k]
+    int* counts;    // [E]
+    int* offsets;   // [E+1]
+    int* tiles;     // [E+1]
+    int* slots;     // [T*k]
+    int* row2tk;    // [P_max]
+    float* wpool;   // [P_max]
+    int* slack;     // [P_max/128]
+    uint8_t* xpool;       // [P_max][H]
+    uint32_t* xpool_sf;   // [NT_max][H/128][128]
+    DevStatus* status;
+};
+
+struct PrepareArgs {
+    const uint8_t* w1;
+    const uint32_t* w1_sf;
+    const uint8_t* w2;
+    const uint32_t* w2_sf;
+    uint8_t* w1p;
+    uint32_t* w1p_sf;
+    uint8_t* w2p;
+    uint32_t* w2p_sf;
+    int H, I, E;
+};
+
+// One grouped GEMM launch (L1: Xpool x W1 with the SwiGLU/requant epilogue;
+// L2: Hpool x W2 with the BF16 epilogue).
+struct GemmArgs {
+    const int* counts;
+    const int* offsets;
+    const int* tiles;
+    int E;
+    int H, I;
+    int tile_n;
+    const uint8_t* sfa;     // prepared weight scales (per 128-row block, per K block)
+    const uint8_t* sfb;     // pool scales (per token tile, per K block)
+    const float* wpool;
+    uint8_t* hpool;         // L1 output [P_max][I]
+    uint8_t* hpool_sf;      // L1 output scales (per token tile, per K block of L2)
+    uint16_t* ypool;        // L2 output [P_max][H]
+    DevStatus* status;
+    uint64_t timeout_ns;
+    int debug_flags;
+    int num_ctas;
+};
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int64_t* idx, float* w,
+                              cudaStream_t stream);
+cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const uint16_t* ypool, const int* slots, int T, int H, int k,
+                           uint16_t* y, cudaStream_t stream);
+cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t stream);
+// layer = 1 or 2; tmap_a over the prepared weights, tmap_b over the pool
+cudaError_t launch_gemm(int layer, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                        const GemmArgs& a, cudaStream_t stream);
+
+}  // namespace moeffn

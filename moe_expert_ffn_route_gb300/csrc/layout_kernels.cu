@@ -1,0 +1,398 @@
+// Routing, schedule-table, gather, combine and weight-preparation kernels
+// of the fused MoE expert forward (everything except the two grouped GEMMs).
+//
+// Sources (page titles as printed, sections):
+//  - MegaMoE blog 4.2 "Dispatch warps": per-expert counting with block-local
+//    atomics over all (token, k) entries, then the pull of each routed
+//    token's hidden vector into the expert pool (here a local gather).
+//  - "Fused comm/compute operators (5): practice", section 2 "schedule
+//    tables": the expert-sorted pool with each expert padded to 128 rows,
+//    the padded prefix, the slot table [token][k] shared by scatter (L1) and
+//    gather-back (L2), the slack per 128-row block, built by a vectorised
+//    GPU builder (one sort + scatter) rather than a host loop.
+//  - MegaMoE code-reading notes, "Stage 6: combine": per token, FP32 sum of
+//    the BF16 expert outputs of its valid top-k slots, cast back to BF16.
+//  - MegaMoE blog 7.3 and the SymmBuffer page section 7 (weight transform:
+//    gate/up interleave by 8 rows, scale transpose for tensor-memory copy).
+#include "common.cuh"
+#include "kernels.h"
+
+#include <cuda_bf16.h>
+
+namespace moeffn {
+
+// ---------------------------------------------------------------------------
+// a0: routing.  One warp per token; lane l holds logits l, l+32, ...
+// ---------------------------------------------------------------------------
+template <int PER_LANE>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
+                                                         int E, int k, int64_t* __restrict__ idx,
+                                                         float* __restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const float* l = logits + static_cast<size_t>(t) * E;
+    float v[PER_LANE];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? __ldg(l + e) : -INFINITY;
+        if (e >= E) taken |= 1u << i;
+    }
+    float my_v = 0.f;
+    int my_e = -1;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) {
+            const int e = lane + 32 * i;
+            if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+                bv = v[i];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == j) {
+            my_v = bv;
+            my_e = be;
+        }
+    }
+    const float top = __shfl_sync(0xffffffffu, my_v, 0);
+    float p = lane < k ? expf(my_v - top) : 0.f;
+    float s = p;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane < k) {
+        idx[static_cast<size_t>(t) * k + lane] = my_e;
+        w[static_cast<size_t>(t) * k + lane] = p / s;
+    }
+}
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int64_t* idx, float* w,
+                              cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int threads = 256, blocks = (T * 32 + threads - 1) / threads;
+    const int per_lane = (E + 31) / 32;
+    if (per_lane <= 2)
+        route_topk_kernel<2><<<blocks, threads, 0, stream>>>(logits, T, E, k, idx, w);
+    else if (per_lane <= 8)
+        route_topk_kernel<8><<<blocks, threads, 0, stream>>>(logits, T, E, k, idx, w);
+    else
+        route_topk_kernel<32><<<blocks, threads, 0, stream>>>(logits, T, E, k, idx, w);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// a1-a3 part 1: per-chunk histograms and stable in-chunk ranks, then (last
+// block) the per-expert chunk bases, counts, 128-row padded offsets and the
+// token-tile prefix.
+// ---------------------------------------------------------------------------
+constexpr int kChunk = 1024;   // (token, k) entries per block
+
+__device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int s = s_warp[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        s_warp[lane] = s;   // inclusive warp totals
+    }
+    __syncthreads();
+    total = s_warp[31];
+    const int before = warp > 0 ? s_warp[warp - 1] : 0;
+    const int r = before + x - v;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kChunk) layout_count_kernel(
+    const int64_t* __restrict__ topk_idx, int N, int E, int tile_n, int* __restrict__ hist,
+    int* __restrict__ rank, int* __restrict__ counts, int* __restrict__ offsets,
+    int* __restrict__ tiles, DevStatus* st) {
+    extern __shared__ int s_wcnt[];   // [32 warps][E]
+    __shared__ int s_warp[32];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < 32 * E; i += kChunk) s_wcnt[i] = 0;
+    __syncthreads();
+
+    const int i = blockIdx.x * kChunk + tid;
+    int e = -1;
+    if (i < N) {
+        const int64_t v = topk_idx[i];
+        if (v >= 0 && v < E)
+            e = static_cast<int>(v);
+        else if (v != -1)
+            atomicOr(&st->code, DEV_ERR_BAD_EXPERT);
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank_in_warp == 0) s_wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    // exclusive scan over the 32 warps for every expert; chunk histogram
+    for (int x = tid; x < E; x += kChunk) {
+        int run = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int c = s_wcnt[w * E + x];
+            s_wcnt[w * E + x] = run;
+            run += c;
+        }
+        hist[static_cast<size_t>(blockIdx.x) * E + x] = run;
+    }
+    __syncthreads();
+    if (i < N) rank[i] = e >= 0 ? s_wcnt[warp * E + e] + rank_in_warp : -1;
+
+    // last block to finish turns the chunk histograms into bases and offsets
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&st->done_counter, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int nchunks = gridDim.x;
+    int cnt = 0;
+    if (tid < E) {
+        int run = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            int* p = hist + static_cast<size_t>(c) * E + tid;
+            const int h = __ldcg(p);
+            *p = run;              // chunk c's first rank inside expert tid
+            run += h;
+        }
+        cnt = run;
+        counts[tid] = cnt;
+    }
+    int total;
+    const int padded = tid < E ? (cnt + kPoolBlock - 1) / kPoolBlock * kPoolBlock : 0;
+    const int off = block_exclusive_scan_1024(padded, s_warp, total);
+    if (tid < E) offsets[tid] = off;
+    if (tid == 0) offsets[E] = total;
+    const int ntile = tid < E ? (cnt + tile_n - 1) / tile_n : 0;
+    const int toff = block_exclusive_scan_1024(ntile, s_warp, total);
+    if (tid < E) tiles[tid] = toff;
+    if (tid == 0) {
+        tiles[E] = total;
+        st->done_counter = 0;   // ready for the next forward on this workspace
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a3 part 2 + a4: slots, inverse map, pool weights, and the gather of token
+// rows and their scales into the expert-sorted pool.  Blocks [0, nb_tok) take
+// 8 tokens each (one warp per token); the remaining blocks fill the padding
+// rows of one expert each.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dispatch_kernel(
+    const uint8_t* __restrict__ x, const uint32_t* __restrict__ x_sf,
+    const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int T, int H, int E,
+    int k, int tile_n, const int* __restrict__ hist, const int* __restrict__ rank,
+    const int* __restrict__ counts, const int* __restrict__ offsets,
+    const int* __restrict__ tiles, int* __restrict__ slots, int* __restrict__ row2tk,
+    float* __restrict__ wpool, int* __restrict__ slack, uint8_t* __restrict__ xpool,
+    uint32_t* __restrict__ xpool_sf, int nb_tok) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (static_cast<int>(blockIdx.x) >= nb_tok) {
+        // padding rows and slack of expert e
+        const int e = blockIdx.x - nb_tok;
+        const int n = counts[e], beg = offsets[e], end = offsets[e + 1];
+        for (int r = beg + n + threadIdx.x; r < end; r += blockDim.x) {
+            row2tk[r] = -1;
+            wpool[r] = 0.f;
+        }
+        for (int b = beg / kPoolBlock + threadIdx.x; b < end / kPoolBlock; b += blockDim.x) {
+            const int real = min(kPoolBlock, max(0, n - (b * kPoolBlock - beg)));
+            slack[b] = kPoolBlock - real;
+        }
+        return;
+    }
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    const int Kb = H / 128;
+    // lane j < k resolves entry (t, j)
+    int slot = -1, chunk = -1, word = 0;
+    if (lane < k) {
+        const int i = t * k + lane;
+        const int64_t v = topk_idx[i];
+        if (v >= 0 && v < E) {
+            const int e = static_cast<int>(v);
+            const int r = hist[static_cast<size_t>(i / kChunk) * E + e] + rank[i];
+            slot = offsets[e] + r;
+            chunk = tiles[e] + r / tile_n;
+            const int rt = r % tile_n;
+            word = (rt & 31) * 4 + (rt >> 5);
+            row2tk[slot] = i;
+            wpool[slot] = topk_w[i];
+        }
+        slots[i] = slot;
+    }
+    // scales: word kb of the token's row goes to chunk `chunk`, K block kb
+    for (int j = 0; j < k; ++j) {
+        const int s = __shfl_sync(0xffffffffu, slot, j);
+        const int c = __shfl_sync(0xffffffffu, chunk, j);
+        const int wd = __shfl_sync(0xffffffffu, word, j);
+        if (s < 0) continue;
+        for (int kb = lane; kb < Kb; kb += 32)
+            xpool_sf[(static_cast<size_t>(c) * Kb + kb) * 128 + wd] = x_sf[static_cast<size_t>(t) * Kb + kb];
+    }
+    // token row: read once, write to each valid slot (16-byte vectors)
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+    const int nv = H / 16;
+    for (int base = 0; base < nv; base += 32 * 4) {
+        uint4 buf[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int vi = base + u * 32 + lane;
+            if (vi < nv) buf[u] = __ldg(src + vi);
+        }
+        for (int j = 0; j < k; ++j) {
+            const int s = __shfl_sync(0xffffffffu, slot, j);
+            if (s < 0) continue;
+            uint4* dst = reinterpret_cast<uint4*>(xpool + static_cast<size_t>(s) * H);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int vi = base + u * 32 + lane;
+                if (vi < nv) dst[vi] = buf[u];
+            }
+        }
+    }
+}
+
+cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
+    const int N = a.T * a.k;
+    const int nchunks = (N + kChunk - 1) / kChunk;
+    const size_t smem = static_cast<size_t>(32) * a.E * sizeof(int);
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t err = cudaFuncSetAttribute(layout_count_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               32 * 1024 * static_cast<int>(sizeof(int)));
+        if (err != cudaSuccess) return err;
+        attr_done = true;
+    }
+    layout_count_kernel<<<nchunks, kChunk, smem, stream>>>(a.topk_idx, N, a.E, a.tile_n, a.hist,
+                                                          a.rank, a.counts, a.offsets, a.tiles,
+                                                          a.status);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const int nb_tok = (a.T + 7) / 8;
+    dispatch_kernel<<<nb_tok + a.E, 256, 0, stream>>>(
+        a.x, a.x_sf, a.topk_idx, a.topk_w, a.T, a.H, a.E, a.k, a.tile_n, a.hist, a.rank,
+        a.counts, a.offsets, a.tiles, a.slots, a.row2tk, a.wpool, a.slack, a.xpool, a.xpool_sf,
+        nb_tok);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// a9: combine.  One block per token; FP32 sum of the BF16 slot rows in j
+// order, rounded to BF16.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ ypool,
+                                                      const int* __restrict__ slots, int H, int k,
+                                                      uint16_t* __restrict__ y) {
+    __shared__ int s_slot[32];
+    const int t = blockIdx.x;
+    if (threadIdx.x < k) s_slot[threadIdx.x] = slots[static_cast<size_t>(t) * k + threadIdx.x];
+    __syncthreads();
+    const int nv = H / 8;
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int s = s_slot[j];
+            if (s < 0) continue;
+            const uint4 q = __ldg(reinterpret_cast<const uint4*>(ypool + static_cast<size_t>(s) * H) + v);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += __uint_as_float(w[i] << 16);
+                acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+            o[i] = *reinterpret_cast<const uint32_t*>(&p);
+        }
+        reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+cudaError_t launch_combine(const uint16_t* ypool, const int* slots, int T, int H, int k,
+                           uint16_t* y, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    combine_kernel<<<T, 128, 0, stream>>>(ypool, slots, H, k, y);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// weight preparation: W1 rows regrouped to [gate 0..I-1 | up 0..I-1] per
+// expert (the interleave-by-8 undone, so that a 128-row A tile holds 128
+// consecutive gate or up channels), W2 copied; scales of both re-laid per
+// 128-row block and 128-wide K block into the tensor-memory copy order
+// (word 4*l + c = row 32*c + l).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int w1_source_row(int p, int I) {
+    const bool up = p >= I;
+    const int c = up ? p - I : p;
+    return 16 * (c / 8) + (c % 8) + (up ? 8 : 0);
+}
+
+__global__ void prepare_rows_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                    int rows_per_expert, int row_bytes, int I, int is_w1) {
+    const int p = blockIdx.x;                 // destination row within expert
+    const int e = blockIdx.y;
+    const int r = is_w1 ? w1_source_row(p, I) : p;
+    const uint4* s = reinterpret_cast<const uint4*>(src + (static_cast<size_t>(e) * rows_per_expert + r) * row_bytes);
+    uint4* d = reinterpret_cast<uint4*>(dst + (static_cast<size_t>(e) * rows_per_expert + p) * row_bytes);
+    for (int v = threadIdx.x; v < row_bytes / 16; v += blockDim.x) d[v] = __ldg(s + v);
+}
+
+__global__ void prepare_sf_kernel(const uint32_t* __restrict__ src, uint32_t* __restrict__ dst,
+                                  int rows_per_expert, int kb_per_row, int I, int is_w1) {
+    // one block per (expert, 128-row block); threads over (kb, word)
+    const int rb = blockIdx.x, e = blockIdx.y;
+    const int nblk = rows_per_expert / 128;
+    for (int i = threadIdx.x; i < kb_per_row * 128; i += blockDim.x) {
+        const int kb = i / 128, wd = i % 128;
+        const int l = wd / 4, c = wd % 4;
+        const int p = rb * 128 + 32 * c + l;
+        const int r = is_w1 ? w1_source_row(p, I) : p;
+        dst[((static_cast<size_t>(e) * nblk + rb) * kb_per_row + kb) * 128 + wd] =
+            src[(static_cast<size_t>(e) * rows_per_expert + r) * kb_per_row + kb];
+    }
+}
+
+cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t stream) {
+    const int H = a.H, I = a.I, E = a.E;
+    prepare_rows_kernel<<<dim3(2 * I, E), 128, 0, stream>>>(a.w1, a.w1p, 2 * I, H / 2, I, 1);
+    prepare_rows_kernel<<<dim3(H, E), 128, 0, stream>>>(a.w2, a.w2p, H, I / 2, I, 0);
+    prepare_sf_kernel<<<dim3(2 * I / 128, E), 256, 0, stream>>>(a.w1_sf, a.w1p_sf, 2 * I, H / 128, I, 1);
+    prepare_sf_kernel<<<dim3(H / 128, E), 256, 0, stream>>>(a.w2_sf, a.w2p_sf, H, I / 128, I, 0);
+    return cudaGetLastError();
+}
+
+}  // namespace moeffn
