@@ -34,6 +34,9 @@ namespace moeffn {
 template <int BN>
 struct GemmCfg {
     static constexpr int A_BYTES = 128 * 128;     // 128 weight rows x 128 K (E2M1, 16-byte padded)
+    // A TMA load of packed E2M1 (16U4_ALIGN16B) signals the packed global
+    // bytes as its transaction count although it fills A_BYTES of shared memory
+    static constexpr int A_TX_BYTES = A_BYTES / 2;
     static constexpr int B_BYTES = BN * 128;      // BN token rows x 128 K (E4M3)
     static constexpr int SF_BYTES = 2048;         // SFA0 | SFA1 | SFB (512 each) | pad
     static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES + SF_BYTES;
@@ -145,7 +148,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint8_t* sfa0 = p.sfa + static_cast<size_t>(a0 / 128) * nkb * 512;
                 const uint8_t* sfa1 = p.sfa + static_cast<size_t>(a1 / 128) * nkb * 512;
                 const uint8_t* sfb = p.sfb + static_cast<size_t>(ti.tile_idx) * nkb * 512;
-                const uint32_t bytes = C::A_BYTES + C::B_BYTES + 1024 + (a1_valid ? C::A_BYTES + 512 : 0);
+                const uint32_t bytes = C::A_TX_BYTES + C::B_BYTES + 1024 + (a1_valid ? C::A_TX_BYTES + 512 : 0);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, p.timeout_ns, p.status, 1)) {
                         ok = false;

@@ -70,6 +70,8 @@ class GpuRun:
     def sf_bytes(self, view: str, rows: np.ndarray, kblocks: int, tabs) -> np.ndarray:
         """UE8M0 codes [len(rows), 4*kblocks] of pool rows from a tile-layout view."""
         raw = self.view(view, torch.uint8)
+        rows = np.asarray(rows, np.int64)
+        assert rows.size == 0 or (rows.min() >= 0 and rows.max() < tabs["P"]), "pool row out of range"
         e_of = np.searchsorted(tabs["offsets"], rows, side="right") - 1
         r = rows - tabs["offsets"][e_of]
         chunk = tabs["tiles"][e_of] + r // self.tile_n
@@ -78,7 +80,15 @@ class GpuRun:
         kb = np.arange(kblocks)
         byte = ((chunk[:, None] * kblocks + kb[None, :]) * 128 + word[:, None]) * 4
         idx = (byte[:, :, None] + np.arange(4)[None, None, :]).reshape(len(rows), -1)
+        assert idx.size == 0 or (idx.min() >= 0 and idx.max() < raw.numel()), "scale index out of range"
         return raw[torch.from_numpy(idx).cuda()].cpu().numpy()
+
+    def pool_rows(self, view: str, rows: np.ndarray, width: int, dtype=torch.uint8) -> np.ndarray:
+        """Rows of a [P_max][width] pool view, indices checked on the host first."""
+        pool = self.view(view, dtype).view(-1, width)
+        rows = np.asarray(rows, np.int64)
+        assert rows.size == 0 or (rows.min() >= 0 and rows.max() < pool.shape[0]), "pool row out of range"
+        return pool[torch.from_numpy(rows).cuda()].cpu().numpy()
 
 
 def upload_weights(inp, prob):
@@ -97,9 +107,8 @@ def compare_l1_codes(gpu_codes, gpu_exp, ref_codes, ref_exp):
     as 32 non-identical codes) and whether every other value is within one
     E4M3 step of the oracle's value at the oracle's scale."""
     from oracle.grouped import _e4m3
-    n = gpu_codes.shape[0]
-    gc = gpu_codes.reshape(n, -1, 32)
-    rc = ref_codes.reshape(n, -1, 32)
+    gc = gpu_codes.reshape(gpu_exp.shape + (32,))
+    rc = ref_codes.reshape(ref_exp.shape + (32,))
     same_scale = gpu_exp == ref_exp
     zero = (gc & 0x7F) == 0
     same = (gc == rc) | (zero & ((rc & 0x7F) == 0))
