@@ -219,6 +219,32 @@ MOEFFN_API moeffn_status moeffn_query(const moeffn_problem* problem, void* works
 MOEFFN_API moeffn_status moeffn_get_device_status(const moeffn_problem* problem, void* workspace,
                                        moeffn_stream stream, uint32_t* detail);
 
+/* Allocation-free schedule tables.  The pages have no counterpart to this
+ * call; it serves callers that cannot allocate device memory at the moment
+ * they need the routing tables: servers that reserve their whole memory
+ * budget at start-up and forbid later allocations, and latency-critical
+ * loops that must not call cudaMalloc/cudaFree because those can
+ * synchronise the device.  It computes the same counts, 128-row padded
+ * offsets and (token, k) -> slot table as moeffn_forward (views COUNTS,
+ * OFFSETS, SLOTS) with no workspace: its scratch is one static device array
+ * of MOEFFN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library keeps until the process exits.
+ *   topk_idx  int64 [T][k]; -1 = empty; other ids outside [0, E) are
+ *             treated as empty (slot -1)
+ *   counts    int32 [E] out;  offsets int32 [E+1] out;  slots int32 [T*k] out
+ * Needs 64 + 4*T*k + 4*ceil(T*k/1024)*E bytes of the static scratch; larger
+ * problems return MOEFFN_ERR_WORKSPACE_TOO_SMALL before anything runs.
+ * Limits on T, E, k as moeffn_route_topk.  Allocates nothing and frees
+ * nothing.  The first call on a device looks up the array's device address
+ * (with that device current); make that first call before any stream
+ * capture.  All calls share the array and it keeps the last call's
+ * contents: calls that overlap on the GPU race and give wrong tables. */
+#define MOEFFN_NOALLOC_SCRATCH_BYTES (4u << 20)
+MOEFFN_API moeffn_status moeffn_schedule_tables_noalloc(const int64_t* topk_idx, int32_t num_tokens,
+                                                        int32_t num_experts, int32_t topk,
+                                                        int32_t* counts, int32_t* offsets,
+                                                        int32_t* slots, moeffn_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

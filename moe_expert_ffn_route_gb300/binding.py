@@ -62,6 +62,8 @@ SIGNATURES = {
                                ctypes.POINTER(c_size_t)]),
     "moeffn_get_device_status": (c_int32, [ctypes.POINTER(Problem), c_void_p, c_void_p,
                                            ctypes.POINTER(ctypes.c_uint32)]),
+    "moeffn_schedule_tables_noalloc": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p,
+                                                 c_void_p, c_void_p]),
 }
 
 
@@ -244,3 +246,13 @@ def device_status(prob: Problem, workspace, stream=None) -> Tuple[int, int, int]
     st = load().moeffn_get_device_status(ctypes.byref(prob), c_void_p(workspace.data_ptr()),
                                          _stream(stream), words)
     return st, words[0], words[1]
+
+
+def schedule_tables_noalloc(topk_idx, num_experts: int, counts, offsets, slots, stream=None) -> None:
+    """Routing tables without any device allocation (see moeffn_schedule_tables_noalloc):
+    fills the caller's counts [E], offsets [E+1] and slots [T*k] int32 tensors."""
+    T, k = topk_idx.shape
+    _check(load().moeffn_schedule_tables_noalloc(_dev(topk_idx, "topk_idx", 8), T, num_experts, k,
+                                                 _dev(counts, "counts", 4), _dev(offsets, "offsets", 4),
+                                                 _dev(slots, "slots", 4), _stream(stream)),
+           "moeffn_schedule_tables_noalloc")
