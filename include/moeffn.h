@@ -71,8 +71,10 @@ typedef void* moeffn_stream;
  *   return MOEFFN_ERR_UNSUPPORTED.
  * fast_math: 0 = expf and IEEE division in SiLU.  Non-zero is not built yet
  *   and returns MOEFFN_ERR_UNSUPPORTED.
- * tile_n: token rows per grouped-GEMM tile: 0 = chosen from T*k/E, or one of
- *   32, 64, 96, 128.
+ * tile_n: most token rows per grouped-GEMM tile, a multiple of 32 in
+ *   [32, 224]; 0 = 32 when T*k/E <= 32, else 224.
+ *   Each expert's rows are split into ceil(n_e/tile_n) equal tiles rounded
+ *   up to 32 rows.
  * wait_timeout_us: limit of every bounded device wait in microseconds;
  *   0 = 2 000 000 (2 s).
  * debug_flags: 0 for normal use.  Test hooks:
@@ -103,11 +105,11 @@ typedef struct moeffn_problem {
 
 /* Views into a workspace after moeffn_forward (for inspection and tests).
  * P_max = align(T*min(k,E) + E*127, 128) pool rows; P = offsets[E] <= P_max
- * rows are in use; NT_max = ceil(T*k/32) + E token tiles.  Pool scale
- * factors are stored per token tile (tile index tiles[e] + n for the n-th
- * tile of expert e, covering pool rows offsets[e] + n*tile_n ...) and per
- * 128-wide K block as 128 uint32 words; word 4*l + c holds the packed scales
- * of tile row 32*c + l. */
+ * rows are in use; NT_max = ceil(T*k/tile_n) + E token tiles.  The n-th tile
+ * of expert e has index tiles[e] + n and covers pool rows offsets[e] +
+ * n*tile_rows[e] onwards.  Pool scale factors are stored per token tile and
+ * per 128-wide K block as 256 uint32 words: word 128*h + 4*l + c holds the
+ * packed scales of tile row 128*h + 32*c + l. */
 typedef enum moeffn_view {
     MOEFFN_VIEW_STATUS = 0,     /* uint32 [16]: [0] error bits, [1] detail */
     MOEFFN_VIEW_COUNTS = 1,     /* int32 [E]: rows routed to each expert */
@@ -118,10 +120,11 @@ typedef enum moeffn_view {
     MOEFFN_VIEW_WPOOL = 6,      /* float [P_max]: top-k weight of a pool row */
     MOEFFN_VIEW_SLACK = 7,      /* int32 [P_max/128]: padding rows per 128-row block */
     MOEFFN_VIEW_XPOOL = 8,      /* uint8 E4M3 [P_max][H]: gathered tokens */
-    MOEFFN_VIEW_XPOOL_SF = 9,   /* uint32 [NT_max][H/128][128]: their scales (tile layout) */
+    MOEFFN_VIEW_XPOOL_SF = 9,   /* uint32 [NT_max][H/128][256]: their scales (tile layout) */
     MOEFFN_VIEW_HPOOL = 10,     /* uint8 E4M3 [P_max][I]: requantised L1 output */
-    MOEFFN_VIEW_HPOOL_SF = 11,  /* uint32 [NT_max][I/128][128]: its scales (tile layout) */
-    MOEFFN_VIEW_YPOOL = 12      /* uint16 BF16 [P_max][H]: L2 output per pool row */
+    MOEFFN_VIEW_HPOOL_SF = 11,  /* uint32 [NT_max][I/128][256]: its scales (tile layout) */
+    MOEFFN_VIEW_YPOOL = 12,     /* uint16 BF16 [P_max][H]: L2 output per pool row */
+    MOEFFN_VIEW_TILE_ROWS = 13  /* int32 [E]: token rows per tile of each expert */
 } moeffn_view;
 
 /* Human-readable name of a status code (host only; never NULL). */
@@ -215,7 +218,12 @@ MOEFFN_API moeffn_status moeffn_query(const moeffn_problem* problem, void* works
 /* Synchronise `stream`, then read the workspace status word written by the
  * last forward on it.  Returns MOEFFN_OK, MOEFFN_ERR_INVALID_ARG (an expert
  * id outside [-1, E) was seen) or MOEFFN_ERR_TIMEOUT (a bounded wait ran
- * out); *detail (optional) receives the raw status words [0] and [1]. */
+ * out); *detail (optional) receives the raw status words [0] and [1].
+ * Word [1] names the first wait that ran out: 1 a TMA producer (stage free),
+ * 2 an MMA warp (accumulator drained), 3 an MMA warp (stage loaded),
+ * 4 the epilogue (accumulator ready), 5 and 6 the end-of-kernel drains of
+ * copies and MMAs, 7 the second CTA of a pair (stage loaded).  With a whole
+ * grid waiting on one failure, which of them expires first is a race. */
 MOEFFN_API moeffn_status moeffn_get_device_status(const moeffn_problem* problem, void* workspace,
                                        moeffn_stream stream, uint32_t* detail);
 

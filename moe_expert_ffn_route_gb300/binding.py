@@ -40,7 +40,8 @@ DEBUG_STARVE_L1 = 1
 DEBUG_DUMP_L1_ACC = 2
 
 VIEWS = {"status": 0, "counts": 1, "offsets": 2, "tiles": 3, "slots": 4, "row2tk": 5, "wpool": 6,
-         "slack": 7, "xpool": 8, "xpool_sf": 9, "hpool": 10, "hpool_sf": 11, "ypool": 12}
+         "slack": 7, "xpool": 8, "xpool_sf": 9, "hpool": 10, "hpool_sf": 11, "ypool": 12,
+         "tile_rows": 13}
 
 # every symbol include/moeffn.h declares: (restype, argtypes)
 SIGNATURES = {

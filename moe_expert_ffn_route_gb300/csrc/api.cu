@@ -22,7 +22,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct WsLayout {
-    size_t status, counts, offsets, tiles, slots, rank, hist, row2tk, wpool, slack;
+    size_t status, counts, offsets, tiles, tile_rows, tile_expert, slots, rank, hist, row2tk, wpool, slack;
     size_t xpool, xpool_sf, hpool, hpool_sf, ypool, total;
     int64_t P_max, NT_max, nchunks;
 };
@@ -37,7 +37,7 @@ moeffn_status check_problem(const moeffn_problem* p) {
     if (p->hidden % 128 != 0 || p->intermediate % 128 != 0) return MOEFFN_ERR_INVALID_ARG;
     if (p->num_experts < 1 || p->num_experts > 1024) return MOEFFN_ERR_INVALID_ARG;
     if (p->topk < 1 || p->topk > p->num_experts || p->topk > 32) return MOEFFN_ERR_INVALID_ARG;
-    if (p->tile_n != 0 && p->tile_n != 32 && p->tile_n != 64 && p->tile_n != 96 && p->tile_n != 128)
+    if (p->tile_n != 0 && (p->tile_n % kTileQuantum != 0 || p->tile_n < kTileQuantum || p->tile_n > kMaxTileN))
         return MOEFFN_ERR_INVALID_ARG;
     if (p->wait_timeout_us < 0) return MOEFFN_ERR_INVALID_ARG;
     if (p->debug_flags & ~(MOEFFN_DEBUG_STARVE_L1 | MOEFFN_DEBUG_DUMP_L1_ACC)) return MOEFFN_ERR_INVALID_ARG;
@@ -53,12 +53,14 @@ moeffn_status check_problem(const moeffn_problem* p) {
     return MOEFFN_OK;
 }
 
+// Most token rows per GEMM tile.  Each expert's rows are split into
+// ceil(n_e / tile_n) equal tiles rounded up to 32 rows.  By default: 32 when
+// an expert expects at most 32 rows (decode-sized batches: narrow stages,
+// more of them in flight), else kMaxTileN (the widest MMAs, fewest tiles).
 int choose_tile_n(const moeffn_problem& p) {
     if (p.tile_n) return p.tile_n;
     const double m = static_cast<double>(p.num_tokens) * p.topk / p.num_experts;
-    if (m <= 32) return 32;
-    if (m <= 64) return 64;
-    return 96;
+    return m <= 32.0 ? 32 : kMaxTileN;
 }
 
 WsLayout ws_layout(const moeffn_problem& p) {
@@ -67,7 +69,8 @@ WsLayout ws_layout(const moeffn_problem& p) {
     const int64_t N = T * k;
     const int64_t kmin = k < E ? k : E;
     L.P_max = static_cast<int64_t>(align_up(static_cast<size_t>(T * kmin + E * (kPoolBlock - 1)), kPoolBlock));
-    L.NT_max = (N + kMinTileN - 1) / kMinTileN + E;
+    const int64_t bn = choose_tile_n(p);
+    L.NT_max = (N + bn - 1) / bn + E;
     L.nchunks = (N + 1023) / 1024;
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -79,6 +82,8 @@ WsLayout ws_layout(const moeffn_problem& p) {
     L.counts = take(4 * E);
     L.offsets = take(4 * (E + 1));
     L.tiles = take(4 * (E + 1));
+    L.tile_rows = take(4 * E);
+    L.tile_expert = take(4 * L.NT_max);
     L.slots = take(4 * N);
     L.rank = take(4 * N);
     L.hist = take(4 * L.nchunks * E);
@@ -86,9 +91,9 @@ WsLayout ws_layout(const moeffn_problem& p) {
     L.wpool = take(4 * L.P_max);
     L.slack = take(4 * (L.P_max / kPoolBlock));
     L.xpool = take(static_cast<size_t>(L.P_max) * H);
-    L.xpool_sf = take(static_cast<size_t>(L.NT_max) * (H / 128) * 512);
+    L.xpool_sf = take(static_cast<size_t>(L.NT_max) * (H / 128) * 1024);
     L.hpool = take(static_cast<size_t>(L.P_max) * I);
-    L.hpool_sf = take(static_cast<size_t>(L.NT_max) * (I / 128) * 512);
+    L.hpool_sf = take(static_cast<size_t>(L.NT_max) * (I / 128) * 1024);
     L.ypool = take(static_cast<size_t>(L.P_max) * H * 2);
     L.total = o;
     return L;
@@ -267,32 +272,38 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
     int* counts = reinterpret_cast<int*>(w + L.counts);
     int* offsets = reinterpret_cast<int*>(w + L.offsets);
     int* tiles = reinterpret_cast<int*>(w + L.tiles);
+    int* tile_rows = reinterpret_cast<int*>(w + L.tile_rows);
+    int* tile_expert = reinterpret_cast<int*>(w + L.tile_expert);
     int* slots = reinterpret_cast<int*>(w + L.slots);
 
     LayoutArgs la{x, x_sf, topk_idx, topk_w, T, H, E, k, tile_n,
                   reinterpret_cast<int*>(w + L.hist), reinterpret_cast<int*>(w + L.rank), counts, offsets,
-                  tiles, slots, reinterpret_cast<int*>(w + L.row2tk), reinterpret_cast<float*>(w + L.wpool),
+                  tiles, tile_rows, tile_expert, slots, reinterpret_cast<int*>(w + L.row2tk), reinterpret_cast<float*>(w + L.wpool),
                   reinterpret_cast<int*>(w + L.slack), w + L.xpool, reinterpret_cast<uint32_t*>(w + L.xpool_sf),
                   status};
     if (launch_layout(la, st) != cudaSuccess || !mark(1)) return MOEFFN_ERR_CUDA;
 
     const PrepLayout PL = prep_layout(*p);
     const uint8_t* pb = static_cast<const uint8_t*>(prepared);
-    CUtensorMap a1, b1, a2, b2;
+    CUtensorMap a1, a2, b1[kNumTokenBoxes], b2[kNumTokenBoxes];
     if (!make_map(&a1, pb + PL.w1p, H, static_cast<uint64_t>(E) * 2 * I, 128, true) ||
-        !make_map(&b1, w + L.xpool, H, L.P_max, tile_n, false) ||
-        !make_map(&a2, pb + PL.w2p, I, static_cast<uint64_t>(E) * H, 128, true) ||
-        !make_map(&b2, w + L.hpool, I, L.P_max, tile_n, false))
+        !make_map(&a2, pb + PL.w2p, I, static_cast<uint64_t>(E) * H, 128, true))
         return MOEFFN_ERR_CUDA;
+    const uint32_t boxes[kNumTokenBoxes] = {16, 32, 64, kMaxTileN / 2};
+    for (int i = 0; i < kNumTokenBoxes; ++i)
+        if (!make_map(&b1[i], w + L.xpool, H, L.P_max, boxes[i], false) ||
+            !make_map(&b2[i], w + L.hpool, I, L.P_max, boxes[i], false))
+            return MOEFFN_ERR_CUDA;
 
     GemmArgs g{};
     g.counts = counts;
     g.offsets = offsets;
     g.tiles = tiles;
+    g.tile_rows = tile_rows;
+    g.tile_expert = tile_expert;
     g.E = E;
     g.H = H;
     g.I = I;
-    g.tile_n = tile_n;
     g.wpool = reinterpret_cast<const float*>(w + L.wpool);
     g.hpool = w + L.hpool;
     g.hpool_sf = w + L.hpool_sf;
@@ -300,7 +311,8 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
     g.status = status;
     g.timeout_ns = static_cast<uint64_t>(p->wait_timeout_us ? p->wait_timeout_us : 2000000) * 1000ull;
     g.debug_flags = p->debug_flags;
-    g.num_ctas = num_sms;
+    g.num_sms = num_sms;
+    g.tile_n = tile_n;
 
     g.sfa = pb + PL.w1p_sf;
     g.sfb = w + L.xpool_sf;
@@ -354,9 +366,10 @@ moeffn_status moeffn_query(const moeffn_problem* p, void* workspace, int32_t vie
         case MOEFFN_VIEW_WPOOL: off = L.wpool; n = 4 * L.P_max; break;
         case MOEFFN_VIEW_SLACK: off = L.slack; n = 4 * (L.P_max / kPoolBlock); break;
         case MOEFFN_VIEW_XPOOL: off = L.xpool; n = static_cast<size_t>(L.P_max) * H; break;
-        case MOEFFN_VIEW_XPOOL_SF: off = L.xpool_sf; n = static_cast<size_t>(L.NT_max) * (H / 128) * 512; break;
+        case MOEFFN_VIEW_XPOOL_SF: off = L.xpool_sf; n = static_cast<size_t>(L.NT_max) * (H / 128) * 1024; break;
         case MOEFFN_VIEW_HPOOL: off = L.hpool; n = static_cast<size_t>(L.P_max) * I; break;
-        case MOEFFN_VIEW_HPOOL_SF: off = L.hpool_sf; n = static_cast<size_t>(L.NT_max) * (I / 128) * 512; break;
+        case MOEFFN_VIEW_HPOOL_SF: off = L.hpool_sf; n = static_cast<size_t>(L.NT_max) * (I / 128) * 1024; break;
+        case MOEFFN_VIEW_TILE_ROWS: off = L.tile_rows; n = 4 * E; break;
         case MOEFFN_VIEW_YPOOL: off = L.ypool; n = static_cast<size_t>(L.P_max) * H * 2; break;
         default: return MOEFFN_ERR_INVALID_ARG;
     }

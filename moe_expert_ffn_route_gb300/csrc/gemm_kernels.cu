@@ -13,17 +13,27 @@
 // L1 epilogue", "TMA loads and the UMMA pipeline" (multi-stage full/empty
 // barriers), "TMEM column allocation" (two accumulators plus scale-factor
 // columns); MegaMoE blog 4.5 "MMA issue" (4 MMAs of K = 32 per 128-wide K
-// block, one scale byte selected per MMA) and 4.6 "Epilogue warps".
+// block, one scale byte selected per MMA; the 2-SM MMA of a CTA pair) and
+// 4.6 "Epilogue warps".
 //
-// GB300 design (not the pages' SM100 kernel): one persistent CTA per SM,
-// 6 warps -- warp 0 issues TMA, warp 1 issues tcgen05.cp/mma from one
-// thread, warps 2..5 drain TMEM.  A tile is two 128-row weight tiles (L1:
-// the gate and the up rows of the same 128 channels; L2: 256 output
-// channels) against one token tile of tile_n rows, so each thread of the
-// epilogue holds gate and up of one channel for every token of the tile.
-// Token tiles never straddle experts; scale factors of a token tile are
-// stored per tile in tensor-memory copy order, so every stage loads one
-// 512-byte scale chunk per operand.
+// GB300 design (not the pages' SM100 kernel):
+//  - Clusters of two CTAs on two SMs run a 2-SM MMA (cta_group::2): M = 256
+//    weight rows (128 staged and accumulated per CTA) x N token columns (N/2
+//    staged per CTA).  Every CTA keeps its own weight-row scales and the
+//    full token-tile scales in its tensor memory.  A stage therefore holds
+//    one 128-row weight tile and half a token tile per SM.
+//  - A block-scaled MMA occupies an SM's tensor core for max(70, N/2)
+//    cycles, so token tiles are wide: each expert's rows are split into
+//    equal tiles of a multiple of 32 rows, at most BN (224, or 32 for
+//    decode-sized batches, where the narrow stages allow 10 in flight).
+//  - Persistent: pair p takes tiles p, p + P, ...; per CTA warp 0 issues TMA,
+//    warp 1 issues the MMAs (leader) or forwards "stage loaded" to the leader
+//    (peer), warps 2..5 drain TMEM.  Two accumulator stages per CTA.
+//  - For L1 a CTA's 128 weight rows are gate and up of 64 channels in bands
+//    of 32; the warps draining the gate and the up band of a channel group
+//    pair up through shared memory for SwiGLU and requantisation.
+//  - Scale factors of a token tile are stored per tile in tensor-memory copy
+//    order (two 512-byte chunks per 128-wide K block).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -31,67 +41,145 @@
 
 namespace moeffn {
 
+// Optional timeline of CTA 0 of layer L (build with -DMOEFFN_TRACE=L): SM
+// clock stamps around every wait and issue of the load, MMA and epilogue roles.
+#ifdef MOEFFN_TRACE
+constexpr int kTraceEvents = 4096;
+// roles 0-2: load, MMA, epilogue of CTA 0; roles 3-4: load, forwarder of CTA 1
+__device__ unsigned long long g_trace[5][kTraceEvents][3];
+__device__ int g_trace_n[5];
+static int g_trace_grid = 0;
+#define TRACE_STAMP(v) (v) = clock64()
+#define TRACE_PUT(role, i, a, b, c)                                                           \
+    do {                                                                                      \
+        const int r_ = (role) + (blockIdx.x == 1 ? 3 : 0);                                    \
+        if (blockIdx.x < 2 && r_ < 5 && LAYER == MOEFFN_TRACE && (i) < kTraceEvents) {         \
+            g_trace[r_][i][0] = (a);                                                          \
+            g_trace[r_][i][1] = (b);                                                          \
+            g_trace[r_][i][2] = (c);                                                          \
+            g_trace_n[r_] = (i) + 1;                                                          \
+        }                                                                                     \
+    } while (0)
+#else
+#define TRACE_STAMP(v) (void)0
+#define TRACE_PUT(role, i, a, b, c) (void)0
+#endif
+
+// warp roles: 0..7 drain TMEM (two warps per lane quarter, alternating 32-column
+// chunks); 8 and 9 issue the MMAs of the even and the odd tiles of the pair
+// (leader) or forward "stage loaded" of those tiles (peer); 10.. issue TMA.
+// A single thread issues tcgen05 and TMA instructions only at a limited rate
+// (about one block-scaled MMA per 100 cycles with its scale copies, a few
+// copies per microsecond), so the work is split: each MMA warp has its own
+// ring of stages and accumulator, and every stage has its own producer warp.
+constexpr int kEpiWarps = 8;
+constexpr int kMmaWarps = 2;
+constexpr int kFirstMmaWarp = 8;
+constexpr int kFirstProducerWarp = kFirstMmaWarp + kMmaWarps;
+constexpr int kMaxProducersPerRing = 5;
+constexpr int kXposeLd = 34;                         // BF16 elements per transpose row
+constexpr int kXposeBytes = 32 * kXposeLd * 2;
+
+// producer warps of a ring of `sr` stages: the largest divisor of sr up to kMaxProducersPerRing
+constexpr int pick_producers(int sr) {
+    int best = 1;
+    for (int p = 1; p <= kMaxProducersPerRing; ++p)
+        if (sr % p == 0) best = p;
+    return best;
+}
+
 template <int BN>
 struct GemmCfg {
-    static constexpr int A_BYTES = 128 * 128;     // 128 weight rows x 128 K (E2M1, 16-byte padded)
-    // A TMA load of packed E2M1 (16U4_ALIGN16B) signals the packed global
-    // bytes as its transaction count although it fills A_BYTES of shared memory
+    static constexpr int BH = BN / 2;                   // token rows staged per CTA, at most
+    static constexpr int A_BYTES = 128 * 128;           // 128 weight rows x 128 K (E2M1, 16-byte padded)
+    // a TMA load of packed E2M1 (16U4_ALIGN16B) signals the packed global bytes
+    // as its transaction count although it fills A_BYTES of shared memory
     static constexpr int A_TX_BYTES = A_BYTES / 2;
-    static constexpr int B_BYTES = BN * 128;      // BN token rows x 128 K (E4M3)
-    static constexpr int SF_BYTES = 2048;         // SFA0 | SFA1 | SFB (512 each) | pad
-    static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES + SF_BYTES;
-    static constexpr int EPI_BYTES = 4 * 32 * 33 * 4;   // per-warp 32x33 float transpose
-    static constexpr int ACC = BN <= 96 ? 2 : 1;        // accumulator stages in TMEM
-    static constexpr int TMEM_NEED = ACC * 2 * BN + 12;
-    static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128
-                                     : TMEM_NEED <= 256 ? 256 : 512;
-    static constexpr int SFA0_COL = ACC * 2 * BN;
-    static constexpr int SFA1_COL = SFA0_COL + 4;
-    static constexpr int SFB_COL = SFA0_COL + 8;
-    static constexpr int MAX_SMEM = 232448;             // 227 KB opt-in per block
-    static constexpr int FIXED = EPI_BYTES + 1024 + 256;
-    static constexpr int STAGES_FIT = (MAX_SMEM - FIXED) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int B_BYTES = BH * 128;
+    static constexpr int SFA_OFF = A_BYTES + B_BYTES;   // 512 B weight-row scales
+    static constexpr int SFB_OFF = SFA_OFF + 512;       // token scales: one 512-byte chunk per 128 tile rows
+    static constexpr int SFB_BYTES = BN <= 128 ? 512 : 1024;
+    static constexpr int STAGE_BYTES = (SFB_OFF + SFB_BYTES + 1023) / 1024 * 1024;
+    // per epilogue warp a 32 x 34 BF16 transpose; per gate/up pair 2 x 32 partial
+    // amax; per pair warp a vote word
+    static constexpr int EPI_BYTES = kEpiWarps * kXposeBytes + (kEpiWarps / 2) * 2 * 32 * 4 + 64;
+    static constexpr int FIXED = 1024 + EPI_BYTES + 256;
+    static constexpr int STAGES_FIT = (232448 - FIXED) / STAGE_BYTES;
+    static constexpr int STAGES_CAP = STAGES_FIT > 12 ? 12 : STAGES_FIT;
+    static constexpr int RING = STAGES_CAP / 2;                // stages per MMA warp
+    static constexpr int STAGES = 2 * RING;
+    static constexpr int PRODUCERS = pick_producers(RING);     // producer warps per ring
+    static constexpr int THREADS = 32 * (kEpiWarps + kMmaWarps + 2 * PRODUCERS);
     static constexpr int SMEM = FIXED + STAGES * STAGE_BYTES;
+    static constexpr int ACC = 2;                       // accumulator stages
+    static constexpr int SF_SET_COLS = 12;              // SFA 4 | SFB 8; per MMA warp two sets alternating by K block
+    static constexpr int SF_COL = ACC * BN;
+    static constexpr int TMEM_NEED = ACC * BN + kMmaWarps * 2 * SF_SET_COLS;
+    static constexpr int TMEM_COLS = TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
     static_assert(TMEM_NEED <= 512, "tensor memory overflow");
-    static_assert(STAGES >= 2, "pipeline too shallow");
-    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 128, "token tile");
+    static_assert(BN % 32 == 0 && BN <= kMaxTileN, "token tile");
+    static_assert(RING >= 2, "pipeline too shallow");
+    static_assert(RING % PRODUCERS == 0, "each producer warp owns whole stages");
+    static_assert(ACC == kMmaWarps, "one accumulator per MMA warp");
 };
+
+// token-tile TMA boxes per CTA (half a tile): 16, 32, 64 and kMaxTileN/2 rows
+__device__ __forceinline__ int box_for_half(int n) {
+    return n <= 16 ? 0 : n <= 32 ? 1 : n <= 64 ? 2 : 3;
+}
+__device__ __forceinline__ int box_half_rows(int box) {
+    return box == 0 ? 16 : box == 1 ? 32 : box == 2 ? 64 : kMaxTileN / 2;
+}
 
 struct TileInfo {
-    int e, cb, tile_idx, row0, nvalid;
+    int e, cb, tile_idx, row0, nvalid, ncols;   // ncols: pair MMA N (the expert's tile rows, a multiple of 32)
 };
 
+// Work items run expert by expert; within an expert, weight-row tile by tile
+// and, inside one, token tile by token tile.  Expert e owns items
+// [tiles[e] * ncb, tiles[e + 1] * ncb), so item t / ncb is one of e's token
+// tiles and the token-tile owner table names e in one load.
 __device__ __forceinline__ TileInfo decode_tile(int t, int ncb, const GemmArgs& p) {
-    int lo = 0, hi = p.E;   // tiles[lo]*ncb <= t < tiles[hi]*ncb
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(p.tiles + mid) * ncb <= t) lo = mid; else hi = mid;
-    }
+    const int lo = __ldg(p.tile_expert + t / ncb);
     TileInfo ti;
     const int t0 = __ldg(p.tiles + lo);
     const int ntb = __ldg(p.tiles + lo + 1) - t0;
     const int local = t - t0 * ncb;
+    const int rows = __ldg(p.tile_rows + lo);
     ti.e = lo;
     ti.cb = local / ntb;
     const int nb = local - ti.cb * ntb;
     ti.tile_idx = t0 + nb;
-    ti.row0 = __ldg(p.offsets + lo) + nb * p.tile_n;
-    ti.nvalid = min(p.tile_n, __ldg(p.counts + lo) - nb * p.tile_n);
+    ti.row0 = __ldg(p.offsets + lo) + nb * rows;
+    ti.nvalid = min(rows, __ldg(p.counts + lo) - nb * rows);
+    ti.ncols = rows;
     return ti;
 }
 
+// the 64 threads of gate/up warp pair pi = 2 * group + pair (warps 2 pi, 2 pi + 1)
+__device__ __forceinline__ void pair_sync(int pi) {
+    switch (pi) {
+        case 0: named_barrier_sync<1>(64); break;
+        case 1: named_barrier_sync<2>(64); break;
+        case 2: named_barrier_sync<3>(64); break;
+        default: named_barrier_sync<4>(64); break;
+    }
+}
+
 template <int LAYER, int BN>
-__global__ void __launch_bounds__(192, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const GemmArgs p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN>::THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+                    const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
     using C = GemmCfg<BN>;
     constexpr int S = C::STAGES, ACC = C::ACC;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (sbase - raw);
-    float* epi = reinterpret_cast<float*>(gbase + S * C::STAGE_BYTES);
+    __nv_bfloat16* xpose = reinterpret_cast<__nv_bfloat16*>(gbase + S * C::STAGE_BYTES);   // [8 warps][32][34]
+    float* pamax = reinterpret_cast<float*>(gbase + S * C::STAGE_BYTES + kEpiWarps * kXposeBytes);   // [4 pairs][2][32]
+    volatile int* pair_ok = reinterpret_cast<volatile int*>(pamax + (kEpiWarps / 2) * 2 * 32);   // [4 pairs][2 warps]
     uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S * C::STAGE_BYTES + C::EPI_BYTES);
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -103,260 +191,372 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_cta_rank();           // 0: leader (issues the MMAs), 1: peer
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full(s), 1);
+            // the leader's "stage full" also waits for the peer's forwarded arrival
+            mbar_init(full(s), rank == 0 ? 2 : 1);
             mbar_init(empty(s), 1);
         }
         for (int a = 0; a < ACC; ++a) {
             mbar_init(tfull(a), 1);
-            mbar_init(tempty(a), 128);
+            mbar_init(tempty(a), 2 * kEpiWarps);         // one arrival per epilogue warp of both CTAs
         }
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, kMmaWarps);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmB0);
+        prefetch_tensormap(&tmB1);
+        prefetch_tensormap(&tmB2);
+        prefetch_tensormap(&tmB3);
     }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
+    if (warp == kFirstMmaWarp) {
+        tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();                                      // both CTAs' barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int ncb = LAYER == 1 ? p.I / 128 : (p.H + 255) / 256;   // weight-row blocks per expert
+    const int npairs = gridDim.x >> 1, pair = blockIdx.x >> 1;
+    const int ncb = LAYER == 1 ? p.I / 128 : (p.H + 255) / 256;   // 256-row weight tiles (pairs) per expert
     const int nkb = LAYER == 1 ? p.H / 128 : p.I / 128;           // 128-wide K blocks
     const int a_rows = LAYER == 1 ? 2 * p.I : p.H;                 // weight rows per expert
     const int total = __ldg(p.tiles + p.E) * ncb;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA
+    if (warp >= kFirstProducerWarp) {
+        // ------------------------------------------------------------ TMA (both CTAs)
+        const int ring = (warp - kFirstProducerWarp) / C::PRODUCERS;
+        const int pw = (warp - kFirstProducerWarp) % C::PRODUCERS;
         if (lane == 0) {
-            int stage = 0;
+            int ls = 0, ntr = 0;                         // stage within the ring
+            (void)ntr;
             uint32_t phase = 0;
-            uint32_t armed[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            const bool starve = LAYER == 1 && (p.debug_flags & 1);
+            uint32_t armed[C::RING] = {};
+            const bool starve = LAYER == 1 && (p.debug_flags & 1) && rank == 0 && ring == 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int t = pair + ring * npairs; t < total && ok; t += 2 * npairs) {
                 const TileInfo ti = decode_tile(t, ncb, p);
-                const int a0 = ti.e * a_rows + ti.cb * (LAYER == 1 ? 128 : 256);
-                const int a1 = a0 + (LAYER == 1 ? p.I : 128);
-                const bool a1_valid = LAYER == 1 || (ti.cb * 256 + 128 < p.H);
-                const uint8_t* sfa0 = p.sfa + static_cast<size_t>(a0 / 128) * nkb * 512;
-                const uint8_t* sfa1 = p.sfa + static_cast<size_t>(a1 / 128) * nkb * 512;
-                const uint8_t* sfb = p.sfb + static_cast<size_t>(ti.tile_idx) * nkb * 512;
-                const uint32_t bytes = C::A_TX_BYTES + C::B_BYTES + 1024 + (a1_valid ? C::A_TX_BYTES + 512 : 0);
+                const int mrow = ti.cb * 256 + 128 * static_cast<int>(rank);   // first weight row of this CTA
+                const bool mine_valid = mrow < a_rows;                          // false only for an L2 tail half
+                const int a0 = ti.e * a_rows + mrow;
+                const int sf_block = (ti.e * a_rows + (mine_valid ? mrow : ti.cb * 256)) / 128;
+                const uint8_t* sfa = p.sfa + static_cast<size_t>(sf_block) * nkb * 512;
+                const uint8_t* sfb = p.sfb + static_cast<size_t>(ti.tile_idx) * nkb * 1024;
+                const int half = ti.ncols / 2;
+                const int box = box_for_half(half);
+                const CUtensorMap* tmB = box == 0 ? &tmB0 : box == 1 ? &tmB1 : box == 2 ? &tmB2 : &tmB3;
+                const int brow = ti.row0 + half * static_cast<int>(rank);
+                const uint32_t bytes = C::A_TX_BYTES + box_half_rows(box) * 128 + 512 + C::SFB_BYTES;
                 for (int kb = 0; kb < nkb; ++kb) {
+                    if (ls % C::PRODUCERS != pw) {
+                        if (++ls == C::RING) {
+                            ls = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
+                    const int stage = ring * C::RING + ls;
+                    unsigned long long c0 = 0, c1 = 0, c2 = 0;
+                    TRACE_STAMP(c0);
                     if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, p.timeout_ns, p.status, 1)) {
                         ok = false;
                         break;
                     }
+                    TRACE_STAMP(c1);
                     const uint32_t sb = sbase + stage * C::STAGE_BYTES;
-                    const uint32_t sf = sb + 2 * C::A_BYTES + C::B_BYTES;
-                    if (!(starve && t == static_cast<int>(blockIdx.x) && kb == 0)) {
+                    if (!(starve && t == pair && kb == 0)) {
                         mbar_arrive_expect_tx(full(stage), bytes);
                         tma_load_2d(sb, &tmA, full(stage), kb * 128, a0);
-                        if (a1_valid) tma_load_2d(sb + C::A_BYTES, &tmA, full(stage), kb * 128, a1);
-                        tma_load_2d(sb + 2 * C::A_BYTES, &tmB, full(stage), kb * 128, ti.row0);
-                        bulk_load(sf, sfa0 + kb * 512, 512, full(stage));
-                        if (a1_valid) bulk_load(sf + 512, sfa1 + kb * 512, 512, full(stage));
-                        bulk_load(sf + 1024, sfb + kb * 512, 512, full(stage));
-                        ++armed[stage];
+                        tma_load_2d(sb + C::A_BYTES, tmB, full(stage), kb * 128, brow);
+                        bulk_load(sb + C::SFA_OFF, sfa + kb * 512, 512, full(stage));
+                        bulk_load(sb + C::SFB_OFF, sfb + kb * 1024, C::SFB_BYTES, full(stage));
+                        ++armed[ls];
                     }
-                    if (++stage == S) {
-                        stage = 0;
+                    TRACE_STAMP(c2);
+                    if (pw == 0 && ring == 0) TRACE_PUT(0, ntr, c0, c1, c2);
+                    ++ntr;
+                    if (++ls == C::RING) {
+                        ls = 0;
                         phase ^= 1u;
                     }
                 }
             }
             // never leave copies in flight into shared memory: wait for the last
-            // arming of every stage to land (immediate on the normal path)
-            for (int s = 0; s < S; ++s)
-                if (armed[s])
-                    mbar_wait_bounded(full(s), (armed[s] - 1u) & 1u, abort_flag, p.timeout_ns, p.status, 5, false);
+            // arming of every owned stage to land (immediate on the normal path)
+            for (int l = 0; l < C::RING; ++l)
+                if (armed[l])
+                    mbar_wait_bounded(full(ring * C::RING + l), (armed[l] - 1u) & 1u, abort_flag, p.timeout_ns,
+                                      p.status, 5, false);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA
-        if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_mx_e2m1_e4m3(128, BN);
-            int stage = 0, it = 0;
+    } else if (warp >= kFirstMmaWarp) {
+        const int ring = warp - kFirstMmaWarp;               // tiles of this parity, accumulator `ring`
+        if (lane == 0 && rank == 1) {
+            // ---------------------------------------------------- forwarder (peer)
+            // in ring order: once this CTA's copies of a stage have landed,
+            // arrive on the leader's barrier of that stage
+            const uint32_t remote_full0 = map_shared_rank(full(0), 0);
+            int ls = 0, ntr = 0;
+            (void)ntr;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-                const TileInfo ti = decode_tile(t, ncb, p);
-                const bool a1_valid = LAYER == 1 || (ti.cb * 256 + 128 < p.H);
-                const int as = it % ACC;
-                const uint32_t ap = static_cast<uint32_t>(it / ACC) & 1u;
-                if (!mbar_wait_bounded(tempty(as), ap ^ 1u, abort_flag, p.timeout_ns, p.status, 2)) break;
-                tc_fence_after();
-                const uint32_t d0 = tmem + static_cast<uint32_t>(as * 2 * BN);
-                const uint32_t d1 = d0 + BN;
+            for (int t = pair + ring * npairs; t < total && ok; t += 2 * npairs) {
                 for (int kb = 0; kb < nkb; ++kb) {
+                    const int stage = ring * C::RING + ls;
+                    unsigned long long c0 = 0, c1 = 0;
+                    TRACE_STAMP(c0);
+                    if (!mbar_wait_bounded(full(stage), phase, abort_flag, p.timeout_ns, p.status, 7)) {
+                        ok = false;
+                        break;
+                    }
+                    TRACE_STAMP(c1);
+                    mbar_arrive_remote_relaxed(remote_full0 + 8u * stage);
+                    if (ring == 0) TRACE_PUT(1, ntr, c0, c1, c1);
+                    ++ntr;
+                    if (++ls == C::RING) {
+                        ls = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        } else if (lane == 0) {
+            // ---------------------------------------------------- MMA (leader)
+            constexpr uint32_t IDESC = idesc_mx_e2m1_e4m3(256, 0);
+            int ls = 0, it = 0, ntr = 0;
+            (void)ntr;
+            uint32_t phase = 0, kiter = 0;
+            bool ok = true;
+            const int as = ring;
+            const uint32_t sf_base = tmem + C::SF_COL + static_cast<uint32_t>(ring * 2 * C::SF_SET_COLS);
+            for (int t = pair + ring * npairs; t < total && ok; t += 2 * npairs, ++it) {
+                const TileInfo ti = decode_tile(t, ncb, p);
+                const uint32_t idesc_n = IDESC | (static_cast<uint32_t>(ti.ncols >> 3) << 17);
+                const bool two_sfb = ti.ncols > 128;
+                const uint32_t ap = static_cast<uint32_t>(it) & 1u;
+                if (!mbar_wait_bounded<true>(tempty(as), ap ^ 1u, abort_flag, p.timeout_ns, p.status, 2)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(as * BN);
+                uint32_t idk[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    idk[k] = idesc_n | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    const int stage = ring * C::RING + ls;
+                    unsigned long long c0 = 0, c1 = 0, c2 = 0;
+                    TRACE_STAMP(c0);
                     if (!mbar_wait_bounded(full(stage), phase, abort_flag, p.timeout_ns, p.status, 3)) {
                         ok = false;
                         break;
                     }
+                    TRACE_STAMP(c1);
                     tc_fence_after();
                     const uint32_t sb = sbase + stage * C::STAGE_BYTES;
-                    const uint32_t sbb = sb + 2 * C::A_BYTES;
-                    const uint32_t sf = sbb + C::B_BYTES;
-                    tc_cp_sf(tmem + C::SFA0_COL, desc_sf_block(sf));
-                    if (a1_valid) tc_cp_sf(tmem + C::SFA1_COL, desc_sf_block(sf + 512));
-                    tc_cp_sf(tmem + C::SFB_COL, desc_sf_block(sf + 1024));
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t idesc = IDESC | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
-                        const uint64_t bdesc = desc_kmajor_sw128(sbb + 32 * k);
-                        const uint32_t acc = (kb | k) != 0;
-                        tc_mma_mx(d0, desc_kmajor_sw128(sb + 32 * k), bdesc, idesc, tmem + C::SFA0_COL,
-                                  tmem + C::SFB_COL, acc);
-                        if (a1_valid)
-                            tc_mma_mx(d1, desc_kmajor_sw128(sb + C::A_BYTES + 32 * k), bdesc, idesc,
-                                      tmem + C::SFA1_COL, tmem + C::SFB_COL, acc);
-                    }
-                    tc_commit(empty(stage));
-                    if (++stage == S) {
-                        stage = 0;
+                    const uint32_t sfs = sf_base + (kiter & 1u) * C::SF_SET_COLS;
+                    ++kiter;
+                    // descriptors of the stage; a K step of 32 bytes adds 2 to the address field
+                    const uint64_t adesc = desc_kmajor_sw128(sb), bdesc = desc_kmajor_sw128(sb + C::A_BYTES);
+                    tc_cp_sf_pair(sfs, desc_sf_block(sb + C::SFA_OFF));
+                    tc_cp_sf_pair(sfs + 4, desc_sf_block(sb + C::SFB_OFF));
+                    if (two_sfb) tc_cp_sf_pair(sfs + 8, desc_sf_block(sb + C::SFB_OFF + 512));
+                    tc_mma_mx_pair(d, adesc, bdesc, idk[0], sfs, sfs + 4, kb != 0);
+                    tc_mma_mx_pair(d, adesc + 2, bdesc + 2, idk[1], sfs, sfs + 4, 1u);
+                    tc_mma_mx_pair(d, adesc + 4, bdesc + 4, idk[2], sfs, sfs + 4, 1u);
+                    tc_mma_mx_pair(d, adesc + 6, bdesc + 6, idk[3], sfs, sfs + 4, 1u);
+                    tc_commit_pair(empty(stage));
+                    TRACE_STAMP(c2);
+                    if (ring == 0) TRACE_PUT(1, ntr, c0, c1, c2);
+                    ++ntr;
+                    if (++ls == C::RING) {
+                        ls = 0;
                         phase ^= 1u;
                     }
                 }
-                if (ok) tc_commit(tfull(as));
+                if (ok) tc_commit_pair(tfull(as));
             }
-            // every MMA issued by this thread is complete before TMEM is freed
-            tc_commit(mma_done);
+            // every MMA issued by the MMA warps is complete before TMEM is freed
+            // (a kernel uses either 1-CTA or 2-CTA tcgen05 forms, never both)
+            tc_commit_pair(mma_done);
             mbar_wait_bounded(mma_done, 0, abort_flag, p.timeout_ns, p.status, 6, false);
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;                      // TMEM lane quarter of this warp
-        float* tb = epi + (warp - 2) * 32 * 33;
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;                              // TMEM lane quarter of this warp
+        const int grp = warp >> 2;                           // chunk parity of this warp
+        const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const uint32_t leader_tempty0 = map_shared_rank(tempty(0), 0);
         int it = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+        for (int t = pair; t < total; t += npairs, ++it) {
             const TileInfo ti = decode_tile(t, ncb, p);
             const int as = it % ACC;
             const uint32_t ap = static_cast<uint32_t>(it / ACC) & 1u;
-            const bool got = mbar_wait_bounded(tfull(as), ap, abort_flag, p.timeout_ns, p.status, 4);
-            if (!__all_sync(0xffffffffu, got)) break;
+            unsigned long long e0 = 0, e1 = 0, e2 = 0;
+            TRACE_STAMP(e0);
+            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(tfull(as), ap, abort_flag, p.timeout_ns,
+                                                                        p.status, 4));
+            if constexpr (LAYER == 1) {
+                // the two warps of a gate/up pair meet at named barriers below, so
+                // they decide together whether to go on (a timeout may reach only one)
+                const int pi = warp >> 1, hs = q & 1;
+                if (lane == 0) pair_ok[pi * 2 + hs] = got ? 1 : 0;
+                pair_sync(pi);
+                const bool both = pair_ok[pi * 2] && pair_ok[pi * 2 + 1];
+                pair_sync(pi);
+                if (!both) break;
+            } else if (!got) {
+                break;
+            }
+            TRACE_STAMP(e1);
             tc_fence_after();
-            const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(as * 2 * BN);
-            for (int j = 0; j < BN / 32; ++j) {
-                if (32 * j >= ti.nvalid) break;
-                const int rloc = 32 * j + lane;
-                const bool valid = rloc < ti.nvalid;
-                const int row = ti.row0 + rloc;
-                if constexpr (LAYER == 1) {
-                    float g[32], u[32];
-                    tmem_ld32(tbase + 32 * j, g);
-                    tmem_ld32(tbase + BN + 32 * j, u);
+            const uint32_t tacc = tq + static_cast<uint32_t>(as * BN);
+            const int nchunks = (ti.nvalid + 31) / 32;
+            const int mrow = ti.cb * 256 + 128 * static_cast<int>(rank);
+            if constexpr (LAYER == 1) {
+                // quarter q holds band q of this CTA's 128 rows: gate (q even) or up
+                // (q odd) of channels cbase + [0, 32), cbase = mrow / 2 + 32 (q / 2)
+                const int pr = q >> 1, hs = q & 1, pi = warp >> 1;
+                __nv_bfloat16* G = xpose + (2 * pi) * 32 * kXposeLd;
+                __nv_bfloat16* U = G + 32 * kXposeLd;
+                float* pam = pamax + pi * 64;
+                const int cbase = mrow / 2 + 32 * pr;
+                for (int j = grp; j < nchunks; j += 2) {
+                    float v[32];
+                    tmem_ld32(tacc + 32 * j, v);
                     if (p.debug_flags & 2) {
                         // test hook: raw FP32 accumulators, [P_max][gate I | up I] floats
                         float* zd = reinterpret_cast<float*>(p.ypool);
-                        const int c = ti.cb * 128 + 32 * q + lane;
-                        for (int n = 0; n < 32 && 32 * j + n < ti.nvalid; ++n) {
-                            const size_t r = static_cast<size_t>(ti.row0 + 32 * j + n) * 2 * p.I;
-                            zd[r + c] = g[n];
-                            zd[r + p.I + c] = u[n];
-                        }
+                        for (int n = 0; n < 32 && 32 * j + n < ti.nvalid; ++n)
+                            zd[static_cast<size_t>(ti.row0 + 32 * j + n) * 2 * p.I + hs * p.I + cbase + lane] = v[n];
                     }
-                    const float wv = valid ? __ldg(p.wpool + row) : 0.f;
+                    // g and u enter SwiGLU rounded to BF16, so the exchange holds BF16
+                    __nv_bfloat16* mine = hs ? U : G;
 #pragma unroll
-                    for (int n = 0; n < 32; ++n) {
-                        const float wn = __shfl_sync(0xffffffffu, wv, n);
-                        const float gb = bf16_round(g[n]);
-                        const float ub = bf16_round(u[n]);
-                        tb[n * 33 + lane] = (gb / (1.0f + expf(-gb))) * ub * wn;
-                    }
-                    __syncwarp();
-                    float v[32];
+                    for (int n = 0; n < 32; ++n) mine[n * kXposeLd + lane] = __float2bfloat16_rn(v[n]);
+                    pair_sync(pi);
+                    // this thread: token 32 j + lane, channels cbase + 16 hs + [0, 16)
+                    const int rloc = 32 * j + lane;
+                    const bool valid = rloc < ti.nvalid;
+                    const int row = ti.row0 + rloc;
+                    const float wv = valid ? __ldg(p.wpool + row) : 0.f;
+                    float h[16];
                     float amax = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        v[i] = tb[lane * 33 + i];
-                        amax = fmaxf(amax, fabsf(v[i]));
+                    for (int i = 0; i < 16; i += 2) {
+                        const float2 g2 = __bfloat1622float2(
+                            *reinterpret_cast<const __nv_bfloat162*>(G + lane * kXposeLd + 16 * hs + i));
+                        const float2 u2 = __bfloat1622float2(
+                            *reinterpret_cast<const __nv_bfloat162*>(U + lane * kXposeLd + 16 * hs + i));
+                        h[i] = (g2.x / (1.0f + expf(-g2.x))) * u2.x * wv;
+                        h[i + 1] = (g2.y / (1.0f + expf(-g2.y))) * u2.y * wv;
+                        amax = fmaxf(amax, fmaxf(fabsf(h[i]), fabsf(h[i + 1])));
                     }
-                    __syncwarp();
+                    pam[hs * 32 + lane] = amax;
+                    pair_sync(pi);
+                    amax = fmaxf(amax, pam[(hs ^ 1) * 32 + lane]);
                     const int ex = requant_exponent(amax);
                     const float s = exp2_neg(ex);
-                    uint32_t pk[8];
+                    uint32_t pk[4];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        pk[i] = e4m3x2(v[4 * i] * s, v[4 * i + 1] * s) |
-                                (e4m3x2(v[4 * i + 2] * s, v[4 * i + 3] * s) << 16);
+                    for (int i = 0; i < 4; ++i)
+                        pk[i] = e4m3x2(h[4 * i] * s, h[4 * i + 1] * s) | (e4m3x2(h[4 * i + 2] * s, h[4 * i + 3] * s) << 16);
                     if (valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(p.hpool + static_cast<size_t>(row) * p.I + ti.cb * 128 + 32 * q);
-                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                        const size_t wd = (static_cast<size_t>(ti.tile_idx) * (p.I / 128) + ti.cb) * 128 +
-                                          (rloc & 31) * 4 + (rloc >> 5);
-                        p.hpool_sf[wd * 4 + q] = static_cast<uint8_t>(ex + 127);
+                        *reinterpret_cast<uint4*>(p.hpool + static_cast<size_t>(row) * p.I + cbase + 16 * hs) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        if (hs == 0) {
+                            // the L2 B-operand scale of this row and 32-channel group
+                            const int kb2 = cbase / 128, byte = (cbase % 128) / 32;
+                            const size_t wd = ((static_cast<size_t>(ti.tile_idx) * (p.I / 128) + kb2) * 2 + (rloc >> 7)) * 128 +
+                                              (rloc & 31) * 4 + ((rloc & 127) >> 5);
+                            p.hpool_sf[wd * 4 + byte] = static_cast<uint8_t>(ex + 127);
+                        }
                     }
-                } else {
-                    const bool a1_valid = ti.cb * 256 + 128 < p.H;
-#pragma unroll 1
-                    for (int half = 0; half < 2; ++half) {
-                        if (half == 1 && !a1_valid) break;
-                        float yv[32];
-                        tmem_ld32(tbase + half * BN + 32 * j, yv);
+                    pair_sync(pi);
+                }
+            } else if (mrow < p.H) {
+                __nv_bfloat16* tb = xpose + warp * 32 * kXposeLd;
+                const int cbase = mrow + 32 * q;
+                for (int j = grp; j < nchunks; j += 2) {
+                    float v[32];
+                    tmem_ld32(tacc + 32 * j, v);
 #pragma unroll
-                        for (int n = 0; n < 32; ++n) tb[n * 33 + lane] = yv[n];
-                        __syncwarp();
-                        uint32_t pk[16];
+                    for (int n = 0; n < 32; ++n) tb[n * kXposeLd + lane] = __float2bfloat16_rn(v[n]);
+                    __syncwarp();
+                    const int rloc = 32 * j + lane;
+                    uint32_t pk[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(tb[lane * 33 + 2 * i], tb[lane * 33 + 2 * i + 1]);
-                            pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
-                        }
-                        __syncwarp();
-                        if (valid) {
-                            uint4* dst = reinterpret_cast<uint4*>(p.ypool + static_cast<size_t>(row) * p.H + ti.cb * 256 + half * 128 + 32 * q);
+                    for (int i = 0; i < 16; ++i) pk[i] = *reinterpret_cast<const uint32_t*>(tb + lane * kXposeLd + 2 * i);
+                    __syncwarp();
+                    if (rloc < ti.nvalid) {
+                        uint4* dst = reinterpret_cast<uint4*>(p.ypool + static_cast<size_t>(ti.row0 + rloc) * p.H + cbase);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                        }
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                     }
                 }
             }
             tc_fence_before();
-            mbar_arrive(tempty(as));
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(leader_tempty0 + 8u * as);
+            TRACE_STAMP(e2);
+            if (warp == 0 && lane == 0) TRACE_PUT(2, it, e0, e1, e2);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    cluster_sync();                                      // no CTA leaves while its pair may still use its memory
+    if (warp == kFirstMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        tmem_dealloc_pair(tmem, C::TMEM_COLS);
     }
 }
 
+#ifdef MOEFFN_TRACE
+extern "C" __attribute__((visibility("default"))) int moeffn_trace_read(unsigned long long* out, int* counts) {
+    if (cudaMemcpyFromSymbol(out, g_trace, sizeof(g_trace)) != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(counts, g_trace_n, sizeof(g_trace_n)) != cudaSuccess) return -1;
+    return g_trace_grid;
+}
+#endif
+
 template <int LAYER, int BN>
-static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap* tmB, const GemmArgs& a,
                               cudaStream_t stream) {
     using C = GemmCfg<BN>;
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<LAYER, BN>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    auto kernel = grouped_gemm_kernel<LAYER, BN>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (err != cudaSuccess) return err;
-    grouped_gemm_kernel<LAYER, BN><<<a.num_ctas, 192, C::SMEM, stream>>>(tmA, tmB, a);
+    // persistent grid: as many CTA pairs as can be resident at once
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (a.num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1) {
+        (void)cudaGetLastError();
+        clusters = a.num_sms / 2;
+    }
+    cfg.gridDim = dim3(2 * (clusters < a.num_sms / 2 ? clusters : a.num_sms / 2), 1, 1);
+#ifdef MOEFFN_TRACE
+    if (LAYER == MOEFFN_TRACE) g_trace_grid = static_cast<int>(cfg.gridDim.x);
+#endif
+    err = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB[0], tmB[1], tmB[2], tmB[3], a);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(int layer, const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm(int layer, const CUtensorMap& tmA, const CUtensorMap* tmB, const GemmArgs& a,
                         cudaStream_t stream) {
-    switch (a.tile_n * 10 + layer) {
-        case 321: return launch_one<1, 32>(tmA, tmB, a, stream);
-        case 322: return launch_one<2, 32>(tmA, tmB, a, stream);
-        case 641: return launch_one<1, 64>(tmA, tmB, a, stream);
-        case 642: return launch_one<2, 64>(tmA, tmB, a, stream);
-        case 961: return launch_one<1, 96>(tmA, tmB, a, stream);
-        case 962: return launch_one<2, 96>(tmA, tmB, a, stream);
-        case 1281: return launch_one<1, 128>(tmA, tmB, a, stream);
-        case 1282: return launch_one<2, 128>(tmA, tmB, a, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    // stage layouts for tiles of at most 32 and kMaxTileN rows (a layout for
+    // 128-row tiles, with 8 narrower stages in flight, measured slower on
+    // 128-row tiles than the kMaxTileN layout's 6 stages)
+    if (a.tile_n <= 32)
+        return layer == 1 ? launch_one<1, 32>(tmA, tmB, a, stream) : launch_one<2, 32>(tmA, tmB, a, stream);
+    return layer == 1 ? launch_one<1, kMaxTileN>(tmA, tmB, a, stream) : launch_one<2, kMaxTileN>(tmA, tmB, a, stream);
 }
 
 }  // namespace moeffn

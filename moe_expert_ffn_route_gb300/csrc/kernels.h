@@ -14,18 +14,20 @@ struct LayoutArgs {
     const uint32_t* x_sf;
     const int64_t* topk_idx;
     const float* topk_w;
-    int T, H, E, k, tile_n;
+    int T, H, E, k, tile_n;   // tile_n: most token rows per GEMM tile
     int* hist;      // [ceil(T*k/1024)][E]
     int* rank;      // [T*k]
     int* counts;    // [E]
     int* offsets;   // [E+1]
-    int* tiles;     // [E+1]
+    int* tiles;     // [E+1] first token tile of each expert
+    int* tile_rows; // [E]   token rows per tile of each expert (multiple of 32)
+    int* tile_expert; // [NT_max] expert of each token tile
     int* slots;     // [T*k]
     int* row2tk;    // [P_max]
     float* wpool;   // [P_max]
     int* slack;     // [P_max/128]
     uint8_t* xpool;       // [P_max][H]
-    uint32_t* xpool_sf;   // [NT_max][H/128][128]
+    uint32_t* xpool_sf;   // [NT_max][H/128][2][128]
     DevStatus* status;
 };
 
@@ -47,9 +49,10 @@ struct GemmArgs {
     const int* counts;
     const int* offsets;
     const int* tiles;
+    const int* tile_rows;
+    const int* tile_expert;  // expert of each token tile
     int E;
     int H, I;
-    int tile_n;
     const uint8_t* sfa;     // prepared weight scales (per 128-row block, per K block)
     const uint8_t* sfb;     // pool scales (per token tile, per K block)
     const float* wpool;
@@ -59,7 +62,8 @@ struct GemmArgs {
     DevStatus* status;
     uint64_t timeout_ns;
     int debug_flags;
-    int num_ctas;
+    int num_sms;
+    int tile_n;             // most token rows per tile (selects the stage layout)
 };
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int64_t* idx, float* w,
@@ -68,8 +72,9 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const uint16_t* ypool, const int* slots, int T, int H, int k,
                            uint16_t* y, cudaStream_t stream);
 cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t stream);
-// layer = 1 or 2; tmap_a over the prepared weights, tmap_b over the pool
-cudaError_t launch_gemm(int layer, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+// layer = 1 or 2; tmap_a over the prepared weights, tmap_b[4] over the pool
+// with boxes of 16, 32, 64 and kMaxTileN/2 token rows (half a pair's tile)
+cudaError_t launch_gemm(int layer, const CUtensorMap& tmap_a, const CUtensorMap* tmap_b,
                         const GemmArgs& a, cudaStream_t stream);
 
 }  // namespace moeffn

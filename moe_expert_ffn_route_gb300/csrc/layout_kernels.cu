@@ -130,7 +130,7 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int
 __global__ void __launch_bounds__(kChunk) layout_count_kernel(
     const int64_t* __restrict__ topk_idx, int N, int E, int tile_n, int* __restrict__ hist,
     int* __restrict__ rank, int* __restrict__ counts, int* __restrict__ offsets,
-    int* __restrict__ tiles, DevStatus* st) {
+    int* __restrict__ tiles, int* __restrict__ tile_rows, DevStatus* st) {
     extern __shared__ int s_wcnt[];   // [32 warps][E]
     __shared__ int s_warp[32];
     __shared__ int s_last;
@@ -189,9 +189,14 @@ __global__ void __launch_bounds__(kChunk) layout_count_kernel(
     const int off = block_exclusive_scan_1024(padded, s_warp, total);
     if (tid < E) offsets[tid] = off;
     if (tid == 0) offsets[E] = total;
+    // tiles of an expert: as few as tile_n allows, equal, a multiple of 16 rows
     const int ntile = tid < E ? (cnt + tile_n - 1) / tile_n : 0;
     const int toff = block_exclusive_scan_1024(ntile, s_warp, total);
-    if (tid < E) tiles[tid] = toff;
+    if (tid < E) {
+        tiles[tid] = toff;
+        const int per = ntile ? (cnt + ntile - 1) / ntile : kTileQuantum;
+        tile_rows[tid] = (per + kTileQuantum - 1) / kTileQuantum * kTileQuantum;
+    }
     if (tid == 0) {
         tiles[E] = total;
         st->done_counter = 0;   // ready for the next forward on this workspace
@@ -207,16 +212,18 @@ __global__ void __launch_bounds__(kChunk) layout_count_kernel(
 __global__ void __launch_bounds__(256) dispatch_kernel(
     const uint8_t* __restrict__ x, const uint32_t* __restrict__ x_sf,
     const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int T, int H, int E,
-    int k, int tile_n, const int* __restrict__ hist, const int* __restrict__ rank,
+    int k, const int* __restrict__ hist, const int* __restrict__ rank,
     const int* __restrict__ counts, const int* __restrict__ offsets,
-    const int* __restrict__ tiles, int* __restrict__ slots, int* __restrict__ row2tk,
+    const int* __restrict__ tiles, const int* __restrict__ tile_rows, int* __restrict__ tile_expert,
+    int* __restrict__ slots, int* __restrict__ row2tk,
     float* __restrict__ wpool, int* __restrict__ slack, uint8_t* __restrict__ xpool,
     uint32_t* __restrict__ xpool_sf, int nb_tok) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (static_cast<int>(blockIdx.x) >= nb_tok) {
-        // padding rows and slack of expert e
+        // padding rows, slack and token-tile owner of expert e
         const int e = blockIdx.x - nb_tok;
         const int n = counts[e], beg = offsets[e], end = offsets[e + 1];
+        for (int tt = tiles[e] + threadIdx.x; tt < tiles[e + 1]; tt += blockDim.x) tile_expert[tt] = e;
         for (int r = beg + n + threadIdx.x; r < end; r += blockDim.x) {
             row2tk[r] = -1;
             wpool[r] = 0.f;
@@ -239,9 +246,11 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
             const int e = static_cast<int>(v);
             const int r = hist[static_cast<size_t>(i / kChunk) * E + e] + rank[i];
             slot = offsets[e] + r;
-            chunk = tiles[e] + r / tile_n;
-            const int rt = r % tile_n;
-            word = (rt & 31) * 4 + (rt >> 5);
+            const int rows = tile_rows[e];
+            chunk = tiles[e] + r / rows;
+            const int rt = r % rows;
+            // 128-row half of the tile, then word 4 l + c for row 32 c + l of that half
+            word = (rt >> 7) * 128 + (rt & 31) * 4 + ((rt & 127) >> 5);
             row2tk[slot] = i;
             wpool[slot] = topk_w[i];
         }
@@ -254,7 +263,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
         const int wd = __shfl_sync(0xffffffffu, word, j);
         if (s < 0) continue;
         for (int kb = lane; kb < Kb; kb += 32)
-            xpool_sf[(static_cast<size_t>(c) * Kb + kb) * 128 + wd] = x_sf[static_cast<size_t>(t) * Kb + kb];
+            xpool_sf[(static_cast<size_t>(c) * Kb + kb) * 256 + wd] = x_sf[static_cast<size_t>(t) * Kb + kb];
     }
     // token row: read once, write to each valid slot (16-byte vectors)
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
@@ -293,14 +302,14 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
     }
     layout_count_kernel<<<nchunks, kChunk, smem, stream>>>(a.topk_idx, N, a.E, a.tile_n, a.hist,
                                                           a.rank, a.counts, a.offsets, a.tiles,
-                                                          a.status);
+                                                          a.tile_rows, a.status);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const int nb_tok = (a.T + 7) / 8;
     dispatch_kernel<<<nb_tok + a.E, 256, 0, stream>>>(
-        a.x, a.x_sf, a.topk_idx, a.topk_w, a.T, a.H, a.E, a.k, a.tile_n, a.hist, a.rank,
-        a.counts, a.offsets, a.tiles, a.slots, a.row2tk, a.wpool, a.slack, a.xpool, a.xpool_sf,
-        nb_tok);
+        a.x, a.x_sf, a.topk_idx, a.topk_w, a.T, a.H, a.E, a.k, a.hist, a.rank,
+        a.counts, a.offsets, a.tiles, a.tile_rows, a.tile_expert, a.slots, a.row2tk, a.wpool, a.slack,
+        a.xpool, a.xpool_sf, nb_tok);
     return cudaGetLastError();
 }
 
@@ -349,16 +358,18 @@ cudaError_t launch_combine(const uint16_t* ypool, const int* slots, int T, int H
 }
 
 // ---------------------------------------------------------------------------
-// weight preparation: W1 rows regrouped to [gate 0..I-1 | up 0..I-1] per
-// expert (the interleave-by-8 undone, so that a 128-row A tile holds 128
-// consecutive gate or up channels), W2 copied; scales of both re-laid per
-// 128-row block and 128-wide K block into the tensor-memory copy order
-// (word 4*l + c = row 32*c + l).
+// weight preparation: W1 rows regrouped so that each 128-row block holds
+// gate and up of 64 consecutive channels in bands of 32 (gate c0..c0+31,
+// up c0..c0+31, gate c0+32..c0+63, up c0+32..c0+63), undoing the boundary's
+// interleave by 8; W2 copied; scales of both re-laid per 128-row block and
+// 128-wide K block into the tensor-memory copy order (word 4*l + c = row
+// 32*c + l).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int w1_source_row(int p, int I) {
-    const bool up = p >= I;
-    const int c = up ? p - I : p;
-    return 16 * (c / 8) + (c % 8) + (up ? 8 : 0);
+    (void)I;
+    const int band = (p % 128) / 32;             // 0 gate lo, 1 up lo, 2 gate hi, 3 up hi
+    const int c = 64 * (p / 128) + 32 * (band >> 1) + (p % 32);
+    return 16 * (c / 8) + (c % 8) + ((band & 1) ? 8 : 0);
 }
 
 __global__ void prepare_rows_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,

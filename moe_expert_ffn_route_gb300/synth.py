@@ -214,7 +214,8 @@ def make_inputs(w: Workload, workers: Optional[int] = None) -> Dict[str, np.ndar
     if workers > 1:
         # spawn: never fork a process that may already hold a CUDA context
         with mp.get_context("spawn").Pool(workers) as pool:
-            results = pool.imap_unordered(_expert, jobs, chunksize=1)
+            # a bounded get: a pool whose workers cannot start raises instead of waiting forever
+            results = pool.map_async(_expert, jobs, chunksize=1).get(timeout=1800)
             for e, a, b, c, d in results:
                 w1[e], w1_sf[e], w2[e], w2_sf[e] = a, b, c, d
     else:

@@ -62,6 +62,7 @@ class GpuRun:
         P = int(off[-1])
         return dict(counts=self.view("counts")[:E].cpu().numpy(), offsets=off,
                     tiles=self.view("tiles")[: E + 1].cpu().numpy(),
+                    tile_rows=self.view("tile_rows")[:E].cpu().numpy(),
                     slots=self.view("slots")[:N].cpu().numpy().reshape(self.T, self.k),
                     row2tk=self.view("row2tk")[:P].cpu().numpy(),
                     slack=self.view("slack")[: P // 128].cpu().numpy(),
@@ -74,11 +75,12 @@ class GpuRun:
         assert rows.size == 0 or (rows.min() >= 0 and rows.max() < tabs["P"]), "pool row out of range"
         e_of = np.searchsorted(tabs["offsets"], rows, side="right") - 1
         r = rows - tabs["offsets"][e_of]
-        chunk = tabs["tiles"][e_of] + r // self.tile_n
-        rt = r % self.tile_n
-        word = (rt % 32) * 4 + rt // 32
+        tr = tabs["tile_rows"][e_of]
+        chunk = tabs["tiles"][e_of] + r // tr
+        rt = r % tr
+        word = (rt // 128) * 128 + (rt % 32) * 4 + (rt % 128) // 32
         kb = np.arange(kblocks)
-        byte = ((chunk[:, None] * kblocks + kb[None, :]) * 128 + word[:, None]) * 4
+        byte = ((chunk[:, None] * kblocks + kb[None, :]) * 256 + word[:, None]) * 4
         idx = (byte[:, :, None] + np.arange(4)[None, None, :]).reshape(len(rows), -1)
         assert idx.size == 0 or (idx.min() >= 0 and idx.max() < raw.numel()), "scale index out of range"
         return raw[torch.from_numpy(idx).cuda()].cpu().numpy()

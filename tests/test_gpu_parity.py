@@ -68,6 +68,8 @@ def test_layout_parity(name):
     assert got["P"] == ref["P"]
     ntile = -(-ref["counts"] // run.tile_n)
     assert np.array_equal(got["tiles"], np.concatenate([[0], np.cumsum(ntile)]))
+    per = np.where(ntile > 0, -(-ref["counts"] // np.maximum(ntile, 1)), 32)
+    assert np.array_equal(got["tile_rows"], -(-per // 32) * 32)
     s = ref["slots"].reshape(-1)
     assert np.array_equal(got["wpool"][s], w.reshape(-1))
     pad = ref["row2tk"] < 0
@@ -151,7 +153,7 @@ def _check_full(inp, idx, w, run):
     assert max_rel <= Y_MAX_REL and mean_rel <= Y_MEAN_REL, (max_rel, mean_rel)
 
 
-@pytest.mark.parametrize("tile_n", [32, 64, 96, 128])
+@pytest.mark.parametrize("tile_n", [32, 64, 96, 128, 160, 192, 224])
 def test_every_token_tile(tile_n):
     inp, idx, w = _small(T=200, E=5, k=2, skew=True)
     run = GpuRun(inp, idx, w, tile_n=tile_n)
@@ -215,7 +217,7 @@ def test_l1_accumulators_match_exact_products():
     fp64 sum of exactly representable products."""
     from oracle.grouped import _dequant_act, _dequant_w
     inp, idx, w = _small(T=70, H=1024, I=256, E=3, k=2, seed=5)
-    for tile_n in (32, 96):
+    for tile_n in (32, 96, 224):
         run = GpuRun(inp, idx, w, tile_n=tile_n, debug_flags=mb.DEBUG_DUMP_L1_ACC)
         tabs = run.tables()
         z = run.view("ypool", torch.float32)[: tabs["P"] * 2 * run.I].view(tabs["P"], 2 * run.I).cpu().numpy()
@@ -238,7 +240,8 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     inp, idx, w = _small(T=64, E=4, k=2)
     run = GpuRun(inp, idx, w, debug_flags=mb.DEBUG_STARVE_L1, wait_timeout_us=20000)
     st, code, detail = run.status()
-    assert st == mb.ERR_TIMEOUT and code & 2 and detail in (1, 2, 3, 4)
+    # any pipeline wait may be the first of the grid to expire (a race), but it is one of them
+    assert st == mb.ERR_TIMEOUT and code & 2 and 1 <= detail <= 7
     # the context is still usable: a normal forward afterwards is correct
     run2 = GpuRun(inp, idx, w)
     assert run2.status()[0] == mb.OK
