@@ -71,10 +71,10 @@ typedef void* moeffn_stream;
  *   return MOEFFN_ERR_UNSUPPORTED.
  * fast_math: 0 = expf and IEEE division in SiLU.  Non-zero is not built yet
  *   and returns MOEFFN_ERR_UNSUPPORTED.
- * tile_n: most token rows per grouped-GEMM tile, a multiple of 32 in
- *   [32, 224]; 0 = 32 when T*k/E <= 32, else 224.
+ * tile_n: most token rows per grouped-GEMM tile, a multiple of 16 in
+ *   [32, 224]; 0 = 32 when T*k/E <= 32, 144 when T*k/E <= 272, else 224.
  *   Each expert's rows are split into ceil(n_e/tile_n) equal tiles rounded
- *   up to 32 rows.
+ *   up to 16 rows.
  * wait_timeout_us: limit of every bounded device wait in microseconds;
  *   0 = 2 000 000 (2 s).
  * debug_flags: 0 for normal use.  Test hooks:

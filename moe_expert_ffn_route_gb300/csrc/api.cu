@@ -37,7 +37,7 @@ moeffn_status check_problem(const moeffn_problem* p) {
     if (p->hidden % 128 != 0 || p->intermediate % 128 != 0) return MOEFFN_ERR_INVALID_ARG;
     if (p->num_experts < 1 || p->num_experts > 1024) return MOEFFN_ERR_INVALID_ARG;
     if (p->topk < 1 || p->topk > p->num_experts || p->topk > 32) return MOEFFN_ERR_INVALID_ARG;
-    if (p->tile_n != 0 && (p->tile_n % kTileQuantum != 0 || p->tile_n < kTileQuantum || p->tile_n > kMaxTileN))
+    if (p->tile_n != 0 && (p->tile_n % kTileQuantum != 0 || p->tile_n < 32 || p->tile_n > kMaxTileN))
         return MOEFFN_ERR_INVALID_ARG;
     if (p->wait_timeout_us < 0) return MOEFFN_ERR_INVALID_ARG;
     if (p->debug_flags & ~(MOEFFN_DEBUG_STARVE_L1 | MOEFFN_DEBUG_DUMP_L1_ACC)) return MOEFFN_ERR_INVALID_ARG;
@@ -54,13 +54,15 @@ moeffn_status check_problem(const moeffn_problem* p) {
 }
 
 // Most token rows per GEMM tile.  Each expert's rows are split into
-// ceil(n_e / tile_n) equal tiles rounded up to 32 rows.  By default: 32 when
+// ceil(n_e / tile_n) equal tiles rounded up to 16 rows.  By default: 32 when
 // an expert expects at most 32 rows (decode-sized batches: narrow stages,
-// more of them in flight), else kMaxTileN (the widest MMAs, fewest tiles).
+// more of them in flight), 144 up to 272 expected rows (most experts then
+// split in two tiles of at most 144 rows, and three accumulators fit in
+// tensor memory), else kMaxTileN (the widest MMAs, fewest tiles).
 int choose_tile_n(const moeffn_problem& p) {
     if (p.tile_n) return p.tile_n;
     const double m = static_cast<double>(p.num_tokens) * p.topk / p.num_experts;
-    return m <= 32.0 ? 32 : kMaxTileN;
+    return m <= 32.0 ? 32 : m <= 272.0 ? 144 : kMaxTileN;
 }
 
 WsLayout ws_layout(const moeffn_problem& p) {
@@ -289,10 +291,9 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
     if (!make_map(&a1, pb + PL.w1p, H, static_cast<uint64_t>(E) * 2 * I, 128, true) ||
         !make_map(&a2, pb + PL.w2p, I, static_cast<uint64_t>(E) * H, 128, true))
         return MOEFFN_ERR_CUDA;
-    const uint32_t boxes[kNumTokenBoxes] = {16, 32, 64, kMaxTileN / 2};
     for (int i = 0; i < kNumTokenBoxes; ++i)
-        if (!make_map(&b1[i], w + L.xpool, H, L.P_max, boxes[i], false) ||
-            !make_map(&b2[i], w + L.hpool, I, L.P_max, boxes[i], false))
+        if (!make_map(&b1[i], w + L.xpool, H, L.P_max, 16 * (i + 1), false) ||
+            !make_map(&b2[i], w + L.hpool, I, L.P_max, 16 * (i + 1), false))
             return MOEFFN_ERR_CUDA;
 
     GemmArgs g{};

@@ -22,13 +22,16 @@
 //    staged per CTA).  Every CTA keeps its own weight-row scales and the
 //    full token-tile scales in its tensor memory.  A stage therefore holds
 //    one 128-row weight tile and half a token tile per SM.
-//  - A block-scaled MMA occupies an SM's tensor core for max(70, N/2)
-//    cycles, so token tiles are wide: each expert's rows are split into
-//    equal tiles of a multiple of 32 rows, at most BN (224, or 32 for
-//    decode-sized batches, where the narrow stages allow 10 in flight).
-//  - Persistent: pair p takes tiles p, p + P, ...; per CTA warp 0 issues TMA,
-//    warp 1 issues the MMAs (leader) or forwards "stage loaded" to the leader
-//    (peer), warps 2..5 drain TMEM.  Two accumulator stages per CTA.
+//  - A block-scaled MMA (K = 32) occupies an SM's tensor core for
+//    max(48, N/2) cycles, but one thread issues one only every ~100-130
+//    cycles (with its scale copies), so token tiles are wide and two warps
+//    issue MMAs: each expert's rows are split into equal tiles of a multiple
+//    of 16 rows, at most BN (224, or 32 for decode-sized batches, where the
+//    narrow stages allow 10 in flight).
+//  - Persistent: pair p takes tiles p, p + P, ...; the even and the odd ones
+//    go to two MMA warps, each with its own ring of stages, every stage with
+//    its own TMA warp; eight warps drain TMEM.  Tiles use accumulator regions
+//    in turn: two of 224 columns, or three of 144 when no tile is wider.
 //  - For L1 a CTA's 128 weight rows are gate and up of 64 channels in bands
 //    of 32; the warps draining the gate and the up band of a channel group
 //    pair up through shared memory for SwiGLU and requantisation.
@@ -88,7 +91,12 @@ constexpr int pick_producers(int sr) {
     return best;
 }
 
-template <int BN>
+// BN: widest token tile of the stage layout; RW: TMEM columns of one
+// accumulator region (the widest tile it holds).  NACC regions are used in
+// turn by the tiles of a pair (tile i -> region i % NACC), so with three or
+// more regions an MMA warp starts its next tile while the epilogue still
+// drains its previous one.
+template <int BN, int RW>
 struct GemmCfg {
     static constexpr int BH = BN / 2;                   // token rows staged per CTA, at most
     static constexpr int A_BYTES = 128 * 128;           // 128 weight rows x 128 K (E2M1, 16-byte padded)
@@ -111,28 +119,33 @@ struct GemmCfg {
     static constexpr int PRODUCERS = pick_producers(RING);     // producer warps per ring
     static constexpr int THREADS = 32 * (kEpiWarps + kMmaWarps + 2 * PRODUCERS);
     static constexpr int SMEM = FIXED + STAGES * STAGE_BYTES;
-    static constexpr int ACC = 2;                       // accumulator stages
     static constexpr int SF_SET_COLS = 12;              // SFA 4 | SFB 8; per MMA warp two sets alternating by K block
-    static constexpr int SF_COL = ACC * BN;
-    static constexpr int TMEM_NEED = ACC * BN + kMmaWarps * 2 * SF_SET_COLS;
+    static constexpr int SF_COLS = kMmaWarps * 2 * SF_SET_COLS;
+    static constexpr int NACC_FIT = (512 - SF_COLS) / RW;
+    static constexpr int NACC = NACC_FIT > 4 ? 4 : NACC_FIT;   // accumulator regions
+    static constexpr int SF_COL = NACC * RW;
+    static constexpr int TMEM_NEED = NACC * RW + SF_COLS;
     static constexpr int TMEM_COLS = TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
     static_assert(TMEM_NEED <= 512, "tensor memory overflow");
-    static_assert(BN % 32 == 0 && BN <= kMaxTileN, "token tile");
+    static_assert(BN % 32 == 0 && BN <= kMaxTileN && RW % kTileQuantum == 0 && RW <= BN, "token tile");
+    static_assert(NACC >= 2, "at least two accumulator regions");
     static_assert(RING >= 2, "pipeline too shallow");
     static_assert(RING % PRODUCERS == 0, "each producer warp owns whole stages");
-    static_assert(ACC == kMmaWarps, "one accumulator per MMA warp");
 };
 
-// token-tile TMA boxes per CTA (half a tile): 16, 32, 64 and kMaxTileN/2 rows
+// token-tile TMA boxes per CTA (half a tile): 16, 32, ..., kMaxTileN / 2 rows
+struct TokenMaps {
+    CUtensorMap m[kNumTokenBoxes];
+};
 __device__ __forceinline__ int box_for_half(int n) {
-    return n <= 16 ? 0 : n <= 32 ? 1 : n <= 64 ? 2 : 3;
+    return n <= 16 ? 0 : (n + 15) / 16 - 1;
 }
 __device__ __forceinline__ int box_half_rows(int box) {
-    return box == 0 ? 16 : box == 1 ? 32 : box == 2 ? 64 : kMaxTileN / 2;
+    return 16 * (box + 1);
 }
 
 struct TileInfo {
-    int e, cb, tile_idx, row0, nvalid, ncols;   // ncols: pair MMA N (the expert's tile rows, a multiple of 32)
+    int e, cb, tile_idx, row0, nvalid, ncols;   // ncols: pair MMA N (the expert's tile rows, a multiple of 16)
 };
 
 // Work items run expert by expert; within an expert, weight-row tile by tile
@@ -166,13 +179,12 @@ __device__ __forceinline__ void pair_sync(int pi) {
     }
 }
 
-template <int LAYER, int BN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN>::THREADS, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-                    const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
-    using C = GemmCfg<BN>;
-    constexpr int S = C::STAGES, ACC = C::ACC;
+template <int LAYER, int BN, int RW>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, RW>::THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TokenMaps tmB,
+                    const GemmArgs p) {
+    using C = GemmCfg<BN, RW>;
+    constexpr int S = C::STAGES, ACC = C::NACC;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -187,7 +199,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     auto tfull = [&](int a) { return bar0 + 8u * (2 * S + a); };
     auto tempty = [&](int a) { return bar0 + 8u * (2 * S + ACC + a); };
     const uint32_t mma_done = bar0 + 8u * (2 * S + 2 * ACC);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * ACC + 1);
+    const uint32_t stagger = bar0 + 8u * (2 * S + 2 * ACC + 1);   // MMA warp 0 is half a tile in
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * ACC + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,13 +216,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             mbar_init(tempty(a), 2 * kEpiWarps);         // one arrival per epilogue warp of both CTAs
         }
         mbar_init(mma_done, kMmaWarps);
+        mbar_init(stagger, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB0);
-        prefetch_tensormap(&tmB1);
-        prefetch_tensormap(&tmB2);
-        prefetch_tensormap(&tmB3);
+        for (int i = 0; i < kNumTokenBoxes; ++i) prefetch_tensormap(&tmB.m[i]);
     }
     if (warp == kFirstMmaWarp) {
         tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -248,7 +259,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint8_t* sfb = p.sfb + static_cast<size_t>(ti.tile_idx) * nkb * 1024;
                 const int half = ti.ncols / 2;
                 const int box = box_for_half(half);
-                const CUtensorMap* tmB = box == 0 ? &tmB0 : box == 1 ? &tmB1 : box == 2 ? &tmB2 : &tmB3;
+                const CUtensorMap* tmBox = &tmB.m[box];
                 const int brow = ti.row0 + half * static_cast<int>(rank);
                 const uint32_t bytes = C::A_TX_BYTES + box_half_rows(box) * 128 + 512 + C::SFB_BYTES;
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -271,7 +282,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (!(starve && t == pair && kb == 0)) {
                         mbar_arrive_expect_tx(full(stage), bytes);
                         tma_load_2d(sb, &tmA, full(stage), kb * 128, a0);
-                        tma_load_2d(sb + C::A_BYTES, tmB, full(stage), kb * 128, brow);
+                        tma_load_2d(sb + C::A_BYTES, tmBox, full(stage), kb * 128, brow);
                         bulk_load(sb + C::SFA_OFF, sfa + kb * 512, 512, full(stage));
                         bulk_load(sb + C::SFB_OFF, sfb + kb * 1024, C::SFB_BYTES, full(stage));
                         ++armed[ls];
@@ -330,16 +341,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             (void)ntr;
             uint32_t phase = 0, kiter = 0;
             bool ok = true;
-            const int as = ring;
             const uint32_t sf_base = tmem + C::SF_COL + static_cast<uint32_t>(ring * 2 * C::SF_SET_COLS);
+            // The two MMA warps finish tiles at the same rate.  Started together they
+            // would finish together and the second would wait for the epilogue to
+            // drain the first's accumulator before its own; half a tile apart, each
+            // accumulator is drained while the other is being filled.
+            bool staggered = ring != 0;
+            if (ring == 1 && !mbar_wait_bounded(stagger, 0, abort_flag, p.timeout_ns, p.status, 2)) ok = false;
             for (int t = pair + ring * npairs; t < total && ok; t += 2 * npairs, ++it) {
                 const TileInfo ti = decode_tile(t, ncb, p);
                 const uint32_t idesc_n = IDESC | (static_cast<uint32_t>(ti.ncols >> 3) << 17);
                 const bool two_sfb = ti.ncols > 128;
-                const uint32_t ap = static_cast<uint32_t>(it) & 1u;
+                const int tord = 2 * it + ring;                // ordinal of this tile in the pair's sequence
+                const int as = tord % ACC;
+                const uint32_t ap = static_cast<uint32_t>(tord / ACC) & 1u;
                 if (!mbar_wait_bounded<true>(tempty(as), ap ^ 1u, abort_flag, p.timeout_ns, p.status, 2)) break;
                 tc_fence_after();
-                const uint32_t d = tmem + static_cast<uint32_t>(as * BN);
+                const uint32_t d = tmem + static_cast<uint32_t>(as * RW);
                 uint32_t idk[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
@@ -367,6 +385,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tc_mma_mx_pair(d, adesc + 4, bdesc + 4, idk[2], sfs, sfs + 4, 1u);
                     tc_mma_mx_pair(d, adesc + 6, bdesc + 6, idk[3], sfs, sfs + 4, 1u);
                     tc_commit_pair(empty(stage));
+                    if (!staggered && kb == nkb / 2) {
+                        mbar_arrive(stagger);
+                        staggered = true;
+                    }
                     TRACE_STAMP(c2);
                     if (ring == 0) TRACE_PUT(1, ntr, c0, c1, c2);
                     ++ntr;
@@ -377,6 +399,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 if (ok) tc_commit_pair(tfull(as));
             }
+            if (!staggered) mbar_arrive(stagger);         // no tile, or left early: release warp 1
             // every MMA issued by the MMA warps is complete before TMEM is freed
             // (a kernel uses either 1-CTA or 2-CTA tcgen05 forms, never both)
             tc_commit_pair(mma_done);
@@ -412,7 +435,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             TRACE_STAMP(e1);
             tc_fence_after();
-            const uint32_t tacc = tq + static_cast<uint32_t>(as * BN);
+            const uint32_t tacc = tq + static_cast<uint32_t>(as * RW);
             const int nchunks = (ti.nvalid + 31) / 32;
             const int mrow = ti.cb * 256 + 128 * static_cast<int>(rank);
             if constexpr (LAYER == 1) {
@@ -522,11 +545,11 @@ extern "C" __attribute__((visibility("default"))) int moeffn_trace_read(unsigned
 }
 #endif
 
-template <int LAYER, int BN>
+template <int LAYER, int BN, int RW>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap* tmB, const GemmArgs& a,
                               cudaStream_t stream) {
-    using C = GemmCfg<BN>;
-    auto kernel = grouped_gemm_kernel<LAYER, BN>;
+    using C = GemmCfg<BN, RW>;
+    auto kernel = grouped_gemm_kernel<LAYER, BN, RW>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (err != cudaSuccess) return err;
     // persistent grid: as many CTA pairs as can be resident at once
@@ -544,7 +567,9 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap* tmB, co
 #ifdef MOEFFN_TRACE
     if (LAYER == MOEFFN_TRACE) g_trace_grid = static_cast<int>(cfg.gridDim.x);
 #endif
-    err = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB[0], tmB[1], tmB[2], tmB[3], a);
+    TokenMaps maps;
+    for (int i = 0; i < kNumTokenBoxes; ++i) maps.m[i] = tmB[i];
+    err = cudaLaunchKernelEx(&cfg, kernel, tmA, maps, a);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -553,10 +578,15 @@ cudaError_t launch_gemm(int layer, const CUtensorMap& tmA, const CUtensorMap* tm
                         cudaStream_t stream) {
     // stage layouts for tiles of at most 32 and kMaxTileN rows (a layout for
     // 128-row tiles, with 8 narrower stages in flight, measured slower on
-    // 128-row tiles than the kMaxTileN layout's 6 stages)
+    // 128-row tiles than the kMaxTileN layout's 6 stages); tiles of at most
+    // 144 rows get three accumulator regions instead of two
     if (a.tile_n <= 32)
-        return layer == 1 ? launch_one<1, 32>(tmA, tmB, a, stream) : launch_one<2, 32>(tmA, tmB, a, stream);
-    return layer == 1 ? launch_one<1, kMaxTileN>(tmA, tmB, a, stream) : launch_one<2, kMaxTileN>(tmA, tmB, a, stream);
+        return layer == 1 ? launch_one<1, 32, 32>(tmA, tmB, a, stream) : launch_one<2, 32, 32>(tmA, tmB, a, stream);
+    if (a.tile_n <= 144)
+        return layer == 1 ? launch_one<1, kMaxTileN, 144>(tmA, tmB, a, stream)
+                          : launch_one<2, kMaxTileN, 144>(tmA, tmB, a, stream);
+    return layer == 1 ? launch_one<1, kMaxTileN, kMaxTileN>(tmA, tmB, a, stream)
+                      : launch_one<2, kMaxTileN, kMaxTileN>(tmA, tmB, a, stream);
 }
 
 }  // namespace moeffn

@@ -20,7 +20,7 @@ struct LayoutArgs {
     int* counts;    // [E]
     int* offsets;   // [E+1]
     int* tiles;     // [E+1] first token tile of each expert
-    int* tile_rows; // [E]   token rows per tile of each expert (multiple of 32)
+    int* tile_rows; // [E]   token rows per tile of each expert (multiple of 16)
     int* tile_expert; // [NT_max] expert of each token tile
     int* slots;     // [T*k]
     int* row2tk;    // [P_max]

@@ -45,7 +45,8 @@ def test_status_strings():
     (dict(k=33, E=64), mb.ERR_INVALID_ARG),
     (dict(T=-1), mb.ERR_INVALID_ARG),
     (dict(tile_n=40), mb.ERR_INVALID_ARG),
-    (dict(tile_n=48), mb.ERR_INVALID_ARG),
+    (dict(tile_n=48), mb.OK),
+    (dict(tile_n=56), mb.ERR_INVALID_ARG),
     (dict(tile_n=16), mb.ERR_INVALID_ARG),
     (dict(tile_n=256), mb.ERR_INVALID_ARG),
     (dict(tile_n=96), mb.OK),
@@ -67,7 +68,8 @@ def test_check_problem(kw, status):
 
 def test_tile_n_choice():
     assert mb.tile_n(mb.problem(128, 7168, 2048, 256, 8)) == 32       # decode: ~4 rows per expert
-    assert mb.tile_n(mb.problem(8192, 7168, 2048, 256, 8)) == 224     # prefill: ~256 rows per expert
+    assert mb.tile_n(mb.problem(8192, 7168, 2048, 256, 8)) == 144     # prefill: ~256 rows per expert
+    assert mb.tile_n(mb.problem(8192, 7168, 2048, 64, 8)) == 224      # ~1024 rows per expert
     assert mb.tile_n(mb.problem(128, 1024, 512, 8, 2, tile_n=128)) == 128
 
 

@@ -68,8 +68,9 @@ def test_layout_parity(name):
     assert got["P"] == ref["P"]
     ntile = -(-ref["counts"] // run.tile_n)
     assert np.array_equal(got["tiles"], np.concatenate([[0], np.cumsum(ntile)]))
-    per = np.where(ntile > 0, -(-ref["counts"] // np.maximum(ntile, 1)), 32)
-    assert np.array_equal(got["tile_rows"], -(-per // 32) * 32)
+    # equal tiles, rounded up to the 16-row quantum of the tile layout
+    per = np.where(ntile > 0, -(-ref["counts"] // np.maximum(ntile, 1)), 16)
+    assert np.array_equal(got["tile_rows"], -(-per // 16) * 16)
     s = ref["slots"].reshape(-1)
     assert np.array_equal(got["wpool"][s], w.reshape(-1))
     pad = ref["row2tk"] < 0
@@ -153,7 +154,7 @@ def _check_full(inp, idx, w, run):
     assert max_rel <= Y_MAX_REL and mean_rel <= Y_MEAN_REL, (max_rel, mean_rel)
 
 
-@pytest.mark.parametrize("tile_n", [32, 64, 96, 128, 160, 192, 224])
+@pytest.mark.parametrize("tile_n", [32, 48, 64, 96, 128, 144, 160, 192, 224])
 def test_every_token_tile(tile_n):
     inp, idx, w = _small(T=200, E=5, k=2, skew=True)
     run = GpuRun(inp, idx, w, tile_n=tile_n)
@@ -217,7 +218,7 @@ def test_l1_accumulators_match_exact_products():
     fp64 sum of exactly representable products."""
     from oracle.grouped import _dequant_act, _dequant_w
     inp, idx, w = _small(T=70, H=1024, I=256, E=3, k=2, seed=5)
-    for tile_n in (32, 96, 224):
+    for tile_n in (32, 96, 144, 224):
         run = GpuRun(inp, idx, w, tile_n=tile_n, debug_flags=mb.DEBUG_DUMP_L1_ACC)
         tabs = run.tables()
         z = run.view("ypool", torch.float32)[: tabs["P"] * 2 * run.I].view(tabs["P"], 2 * run.I).cpu().numpy()
