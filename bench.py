@@ -69,7 +69,9 @@ def algorithmic(wl, counts):
 
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while running."""
+    """nvidia-smi samples every 20 ms (as fast as it answers) while running.
+    Entering waits for the first sample, so the samples taken between enter
+    and exit fall inside the caller's timed region."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -83,10 +85,14 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.perf_counter()
+            while not self.lines and time.perf_counter() - t0 < 5.0 and self.proc.poll() is None:
+                time.sleep(0.005)
+            self.lines = []
         except OSError:
             self.proc = None
         return self
