@@ -242,7 +242,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // ------------------------------------------------------------ TMA (both CTAs)
         const int ring = (warp - kFirstProducerWarp) / C::PRODUCERS;
         const int pw = (warp - kFirstProducerWarp) % C::PRODUCERS;
-        if (lane == 0) {
+        {
+            // the whole warp runs the loop; one elected lane issues each copy
             int ls = 0, ntr = 0;                         // stage within the ring
             (void)ntr;
             uint32_t phase = 0;
@@ -273,22 +274,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const int stage = ring * C::RING + ls;
                     unsigned long long c0 = 0, c1 = 0, c2 = 0;
                     TRACE_STAMP(c0);
-                    if (!mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag, p.timeout_ns, p.status, 1)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag,
+                                                                    p.timeout_ns, p.status, 1))) {
                         ok = false;
                         break;
                     }
                     TRACE_STAMP(c1);
                     const uint32_t sb = sbase + stage * C::STAGE_BYTES;
                     if (!(starve && t == pair && kb == 0)) {
-                        mbar_arrive_expect_tx(full(stage), bytes);
-                        tma_load_2d(sb, &tmA, full(stage), kb * 128, a0);
-                        tma_load_2d(sb + C::A_BYTES, tmBox, full(stage), kb * 128, brow);
-                        bulk_load(sb + C::SFA_OFF, sfa + kb * 512, 512, full(stage));
-                        bulk_load(sb + C::SFB_OFF, sfb + kb * 1024, C::SFB_BYTES, full(stage));
+                        mbar_arrive_expect_tx_w(full(stage), bytes);
+                        tma_load_2d_w(sb, &tmA, full(stage), kb * 128, a0);
+                        tma_load_2d_w(sb + C::A_BYTES, tmBox, full(stage), kb * 128, brow);
+                        bulk_load_w(sb + C::SFA_OFF, sfa + kb * 512, 512, full(stage));
+                        bulk_load_w(sb + C::SFB_OFF, sfb + kb * 1024, C::SFB_BYTES, full(stage));
                         ++armed[ls];
                     }
                     TRACE_STAMP(c2);
-                    if (pw == 0 && ring == 0) TRACE_PUT(0, ntr, c0, c1, c2);
+                    if (lane == 0 && pw == 0 && ring == 0) TRACE_PUT(0, ntr, c0, c1, c2);
                     ++ntr;
                     if (++ls == C::RING) {
                         ls = 0;
@@ -334,8 +336,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 }
             }
-        } else if (lane == 0) {
+        } else if (rank == 0) {
             // ---------------------------------------------------- MMA (leader)
+            // the whole warp runs the loop; one elected lane issues each instruction
             constexpr uint32_t IDESC = idesc_mx_e2m1_e4m3(256, 0);
             int ls = 0, it = 0, ntr = 0;
             (void)ntr;
@@ -347,7 +350,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             // drain the first's accumulator before its own; half a tile apart, each
             // accumulator is drained while the other is being filled.
             bool staggered = ring != 0;
-            if (ring == 1 && !mbar_wait_bounded(stagger, 0, abort_flag, p.timeout_ns, p.status, 2)) ok = false;
+            if (ring == 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(stagger, 0, abort_flag, p.timeout_ns, p.status, 2)))
+                ok = false;
             for (int t = pair + ring * npairs; t < total && ok; t += 2 * npairs, ++it) {
                 const TileInfo ti = decode_tile(t, ncb, p);
                 const uint32_t idesc_n = IDESC | (static_cast<uint32_t>(ti.ncols >> 3) << 17);
@@ -355,7 +359,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int tord = 2 * it + ring;                // ordinal of this tile in the pair's sequence
                 const int as = tord % ACC;
                 const uint32_t ap = static_cast<uint32_t>(tord / ACC) & 1u;
-                if (!mbar_wait_bounded<true>(tempty(as), ap ^ 1u, abort_flag, p.timeout_ns, p.status, 2)) break;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded<true>(tempty(as), ap ^ 1u, abort_flag, p.timeout_ns,
+                                                                     p.status, 2)))
+                    break;
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(as * RW);
                 uint32_t idk[4];
@@ -366,7 +372,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const int stage = ring * C::RING + ls;
                     unsigned long long c0 = 0, c1 = 0, c2 = 0;
                     TRACE_STAMP(c0);
-                    if (!mbar_wait_bounded(full(stage), phase, abort_flag, p.timeout_ns, p.status, 3)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(full(stage), phase, abort_flag, p.timeout_ns,
+                                                                    p.status, 3))) {
                         ok = false;
                         break;
                     }
@@ -377,32 +384,32 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     ++kiter;
                     // descriptors of the stage; a K step of 32 bytes adds 2 to the address field
                     const uint64_t adesc = desc_kmajor_sw128(sb), bdesc = desc_kmajor_sw128(sb + C::A_BYTES);
-                    tc_cp_sf_pair(sfs, desc_sf_block(sb + C::SFA_OFF));
-                    tc_cp_sf_pair(sfs + 4, desc_sf_block(sb + C::SFB_OFF));
-                    if (two_sfb) tc_cp_sf_pair(sfs + 8, desc_sf_block(sb + C::SFB_OFF + 512));
-                    tc_mma_mx_pair(d, adesc, bdesc, idk[0], sfs, sfs + 4, kb != 0);
-                    tc_mma_mx_pair(d, adesc + 2, bdesc + 2, idk[1], sfs, sfs + 4, 1u);
-                    tc_mma_mx_pair(d, adesc + 4, bdesc + 4, idk[2], sfs, sfs + 4, 1u);
-                    tc_mma_mx_pair(d, adesc + 6, bdesc + 6, idk[3], sfs, sfs + 4, 1u);
-                    tc_commit_pair(empty(stage));
+                    tc_cp_sf_pair_w(sfs, desc_sf_block(sb + C::SFA_OFF));
+                    tc_cp_sf_pair_w(sfs + 4, desc_sf_block(sb + C::SFB_OFF));
+                    if (two_sfb) tc_cp_sf_pair_w(sfs + 8, desc_sf_block(sb + C::SFB_OFF + 512));
+                    tc_mma_mx_pair_w(d, adesc, bdesc, idk[0], sfs, sfs + 4, kb != 0);
+                    tc_mma_mx_pair_w(d, adesc + 2, bdesc + 2, idk[1], sfs, sfs + 4, 1u);
+                    tc_mma_mx_pair_w(d, adesc + 4, bdesc + 4, idk[2], sfs, sfs + 4, 1u);
+                    tc_mma_mx_pair_w(d, adesc + 6, bdesc + 6, idk[3], sfs, sfs + 4, 1u);
+                    tc_commit_pair_w(empty(stage));
                     if (!staggered && kb == nkb / 2) {
-                        mbar_arrive(stagger);
+                        if (lane == 0) mbar_arrive(stagger);
                         staggered = true;
                     }
                     TRACE_STAMP(c2);
-                    if (ring == 0) TRACE_PUT(1, ntr, c0, c1, c2);
+                    if (lane == 0 && ring == 0) TRACE_PUT(1, ntr, c0, c1, c2);
                     ++ntr;
                     if (++ls == C::RING) {
                         ls = 0;
                         phase ^= 1u;
                     }
                 }
-                if (ok) tc_commit_pair(tfull(as));
+                if (ok) tc_commit_pair_w(tfull(as));
             }
-            if (!staggered) mbar_arrive(stagger);         // no tile, or left early: release warp 1
+            if (!staggered && lane == 0) mbar_arrive(stagger);   // no tile, or left early: release warp 9
             // every MMA issued by the MMA warps is complete before TMEM is freed
             // (a kernel uses either 1-CTA or 2-CTA tcgen05 forms, never both)
-            tc_commit_pair(mma_done);
+            tc_commit_pair_w(mma_done);
             mbar_wait_bounded(mma_done, 0, abort_flag, p.timeout_ns, p.status, 6, false);
         }
         __syncwarp();
