@@ -173,6 +173,24 @@ def setup_dist():
     return world, rank, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks of the process group (the value
+    itself without one): the job is as slow as its slowest replica."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, max_ms: float) -> float:
+    """Units per second of the whole job: every replica processes
+    `units_per_rank` units; the job takes the slowest replica's time."""
+    return units_per_rank * world / (max_ms / 1e3)
+
+
 def run_reference(args, wl):
     """--impl reference: the oracle, timed on this host's cores (rank 0 only)."""
     world, rank, _ = setup_dist()
@@ -288,15 +306,11 @@ def main():
         wall = time.perf_counter() - wall0
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     stage_ms = np.array([[ev[j].elapsed_time(ev[j + 1]) for j in range(4)] for ev in stages])
-    total_ms = float(sum(step_ms))
+    total_ms = max_over_ranks(float(sum(step_ms)), dev)
     if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
         torch.distributed.barrier()
     ms_per_step = total_ms / K
-    tokens = T * K * world
-    value = tokens / (total_ms / 1e3)
+    value = whole_job_rate(T * K, world, total_ms)
 
     # e2e through host buffers: pinned inputs -> device, route + forward, y -> pinned host
     h_logits = torch.from_numpy(inp["logits"]).pin_memory()
@@ -317,10 +331,7 @@ def main():
         e_e.record(stream)
         torch.cuda.synchronize()
         e2e_ms += e_s.elapsed_time(e_e)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     if rank != 0:
         if world > 1:
@@ -358,7 +369,7 @@ def main():
         "stage_ms": {"tables+gather": float(stage_ms[:, 0].mean()), "l1_gemm": l1_ms, "l2_gemm": l2_ms,
                      "combine": float(stage_ms[:, 3].mean())},
         "roofline": roof,
-        "e2e": {"value": T * K * world / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rate(T * K, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": KERNELS_PER_STEP * K,
         "wall_s": wall,

@@ -199,8 +199,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     auto tfull = [&](int a) { return bar0 + 8u * (2 * S + a); };
     auto tempty = [&](int a) { return bar0 + 8u * (2 * S + ACC + a); };
     const uint32_t mma_done = bar0 + 8u * (2 * S + 2 * ACC);
-    const uint32_t stagger = bar0 + 8u * (2 * S + 2 * ACC + 1);   // MMA warp 0 is half a tile in
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * ACC + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * ACC + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -216,7 +215,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             mbar_init(tempty(a), 2 * kEpiWarps);         // one arrival per epilogue warp of both CTAs
         }
         mbar_init(mma_done, kMmaWarps);
-        mbar_init(stagger, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA);
@@ -345,13 +343,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t phase = 0, kiter = 0;
             bool ok = true;
             const uint32_t sf_base = tmem + C::SF_COL + static_cast<uint32_t>(ring * 2 * C::SF_SET_COLS);
-            // The two MMA warps finish tiles at the same rate.  Started together they
-            // would finish together and the second would wait for the epilogue to
-            // drain the first's accumulator before its own; half a tile apart, each
-            // accumulator is drained while the other is being filled.
-            bool staggered = ring != 0;
-            if (ring == 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(stagger, 0, abort_flag, p.timeout_ns, p.status, 2)))
-                ok = false;
             for (int t = pair + ring * npairs; t < total && ok; t += 2 * npairs, ++it) {
                 const TileInfo ti = decode_tile(t, ncb, p);
                 const uint32_t idesc_n = IDESC | (static_cast<uint32_t>(ti.ncols >> 3) << 17);
@@ -392,10 +383,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tc_mma_mx_pair_w(d, adesc + 4, bdesc + 4, idk[2], sfs, sfs + 4, 1u);
                     tc_mma_mx_pair_w(d, adesc + 6, bdesc + 6, idk[3], sfs, sfs + 4, 1u);
                     tc_commit_pair_w(empty(stage));
-                    if (!staggered && kb == nkb / 2) {
-                        if (lane == 0) mbar_arrive(stagger);
-                        staggered = true;
-                    }
                     TRACE_STAMP(c2);
                     if (lane == 0 && ring == 0) TRACE_PUT(1, ntr, c0, c1, c2);
                     ++ntr;
@@ -406,7 +393,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 if (ok) tc_commit_pair_w(tfull(as));
             }
-            if (!staggered && lane == 0) mbar_arrive(stagger);   // no tile, or left early: release warp 9
             // every MMA issued by the MMA warps is complete before TMEM is freed
             // (a kernel uses either 1-CTA or 2-CTA tcgen05 forms, never both)
             tc_commit_pair_w(mma_done);
