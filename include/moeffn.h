@@ -69,7 +69,9 @@ typedef void* moeffn_stream;
  * act_clamp: optional activation clamp of the L1 epilogue (MegaMoE notes,
  *   "Activation clamp"); <= 0 disables it.  Values > 0 are not built yet and
  *   return MOEFFN_ERR_UNSUPPORTED.
- * fast_math: 0 = expf and IEEE division in SiLU.  Non-zero is not built yet
+ * fast_math: 0 = expf and a correctly rounded quotient in SiLU (Markstein's
+ *   division method, checked bit for bit against IEEE division on the GPU over
+ *   the SiLU inputs).  Non-zero is not built yet
  *   and returns MOEFFN_ERR_UNSUPPORTED.
  * tile_n: most token rows per grouped-GEMM tile, a multiple of 16 in
  *   [32, 224]; 0 = 32 when T*k/E <= 32, 144 when T*k/E <= 272, else 224.

@@ -292,8 +292,8 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
         !make_map(&a2, pb + PL.w2p, I, static_cast<uint64_t>(E) * H, 128, true))
         return MOEFFN_ERR_CUDA;
     for (int i = 0; i < kNumTokenBoxes; ++i)
-        if (!make_map(&b1[i], w + L.xpool, H, L.P_max, 16 * (i + 1), false) ||
-            !make_map(&b2[i], w + L.hpool, I, L.P_max, 16 * (i + 1), false))
+        if (!make_map(&b1[i], w + L.xpool, H, L.P_max, 8 * (i + 1), false) ||
+            !make_map(&b2[i], w + L.hpool, I, L.P_max, 8 * (i + 1), false))
             return MOEFFN_ERR_CUDA;
 
     GemmArgs g{};

@@ -68,20 +68,22 @@ static int g_trace_grid = 0;
 #define TRACE_PUT(role, i, a, b, c) (void)0
 #endif
 
-// warp roles: 0..7 drain TMEM (two warps per lane quarter, alternating 32-column
-// chunks); 8 and 9 issue the MMAs of the even and the odd tiles of the pair
-// (leader) or forward "stage loaded" of those tiles (peer); 10.. issue TMA.
-// A single thread issues tcgen05 and TMA instructions only at a limited rate
-// (about one block-scaled MMA per 100 cycles with its scale copies, a few
-// copies per microsecond), so the work is split: each MMA warp has its own
-// ring of stages and accumulator, and every stage has its own producer warp.
-constexpr int kEpiWarps = 8;
+// warp roles: 0..11 drain TMEM (three warps per lane quarter, taking every
+// third 32-column chunk); 12 and 13 issue the MMAs of the even and the odd
+// tiles of the pair (leader) or forward "stage loaded" of those tiles (peer);
+// 14 and 15 issue the TMA copies of the two rings of stages.  The MMA and TMA
+// warps issue from all 32 lanes through elect.sync: issued from one lane of a
+// divergent branch a block-scaled MMA costs about twice its tensor-pipe time.
+constexpr int kEpiWarps = 12;
+constexpr int kEpiGroups = kEpiWarps / 4;
 constexpr int kMmaWarps = 2;
-constexpr int kFirstMmaWarp = 8;
+constexpr int kFirstMmaWarp = kEpiWarps;
 constexpr int kFirstProducerWarp = kFirstMmaWarp + kMmaWarps;
-constexpr int kMaxProducersPerRing = 5;
-constexpr int kXposeLd = 34;                         // BF16 elements per transpose row
-constexpr int kXposeBytes = 32 * kXposeLd * 2;
+constexpr int kMaxProducersPerRing = 1;
+// L1 epilogue: the gate and the up warp of a channel group hand each other one
+// half of a 32-token chunk through a 32-channel x 16-token BF16 buffer
+constexpr int kXchLd = 18;                           // BF16 per buffer row: 16 tokens + 2 padding
+constexpr int kXchElems = 32 * kXchLd;
 
 // producer warps of a ring of `sr` stages: the largest divisor of sr up to kMaxProducersPerRing
 constexpr int pick_producers(int sr) {
@@ -104,21 +106,24 @@ struct GemmCfg {
     // as its transaction count although it fills A_BYTES of shared memory
     static constexpr int A_TX_BYTES = A_BYTES / 2;
     static constexpr int B_BYTES = BH * 128;
-    static constexpr int SFA_OFF = A_BYTES + B_BYTES;   // 512 B weight-row scales
-    static constexpr int SFB_OFF = SFA_OFF + 512;       // token scales: one 512-byte chunk per 128 tile rows
+    // operand tiles of a stage, 1024-byte aligned for the 128-byte swizzle
+    static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES + 1023) / 1024 * 1024;
+    // scales of a stage, kept apart from the tiles: 512 B weight-row scales,
+    // then one 512-byte chunk of token scales per 128 tile rows
     static constexpr int SFB_BYTES = BN <= 128 ? 512 : 1024;
-    static constexpr int STAGE_BYTES = (SFB_OFF + SFB_BYTES + 1023) / 1024 * 1024;
-    // per epilogue warp a 32 x 34 BF16 transpose; per gate/up pair 2 x 32 partial
-    // amax; per pair warp a vote word
-    static constexpr int EPI_BYTES = kEpiWarps * kXposeBytes + (kEpiWarps / 2) * 2 * 32 * 4 + 64;
+    static constexpr int SF_STAGE = 512 + SFB_BYTES;
+    // per gate/up warp pair two BF16 exchange buffers (L2: one staging buffer per
+    // epilogue warp in the same bytes); per pair warp a vote word
+    static constexpr int XCH_BYTES = (kEpiWarps / 2) * 2 * kXchElems * 2;
+    static constexpr int EPI_BYTES = XCH_BYTES + 4 * kEpiWarps;
     static constexpr int FIXED = 1024 + EPI_BYTES + 256;
-    static constexpr int STAGES_FIT = (232448 - FIXED) / STAGE_BYTES;
+    static constexpr int STAGES_FIT = (232448 - FIXED) / (STAGE_BYTES + SF_STAGE);
     static constexpr int STAGES_CAP = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr int RING = STAGES_CAP / 2;                // stages per MMA warp
     static constexpr int STAGES = 2 * RING;
     static constexpr int PRODUCERS = pick_producers(RING);     // producer warps per ring
     static constexpr int THREADS = 32 * (kEpiWarps + kMmaWarps + 2 * PRODUCERS);
-    static constexpr int SMEM = FIXED + STAGES * STAGE_BYTES;
+    static constexpr int SMEM = FIXED + STAGES * (STAGE_BYTES + SF_STAGE);
     static constexpr int SF_SET_COLS = 12;              // SFA 4 | SFB 8; per MMA warp two sets alternating by K block
     static constexpr int SF_COLS = kMmaWarps * 2 * SF_SET_COLS;
     static constexpr int NACC_FIT = (512 - SF_COLS) / RW;
@@ -127,21 +132,22 @@ struct GemmCfg {
     static constexpr int TMEM_NEED = NACC * RW + SF_COLS;
     static constexpr int TMEM_COLS = TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
     static_assert(TMEM_NEED <= 512, "tensor memory overflow");
-    static_assert(BN % 32 == 0 && BN <= kMaxTileN && RW % kTileQuantum == 0 && RW <= BN, "token tile");
+    static_assert(BN % 16 == 0 && BN <= kMaxTileN && RW % kTileQuantum == 0 && RW <= BN, "token tile");
+    static_assert(SMEM <= 232448, "shared memory");
     static_assert(NACC >= 2, "at least two accumulator regions");
     static_assert(RING >= 2, "pipeline too shallow");
     static_assert(RING % PRODUCERS == 0, "each producer warp owns whole stages");
 };
 
-// token-tile TMA boxes per CTA (half a tile): 16, 32, ..., kMaxTileN / 2 rows
+// token-tile TMA boxes per CTA (half a tile): 8, 16, ..., kMaxTileN / 2 rows
 struct TokenMaps {
     CUtensorMap m[kNumTokenBoxes];
 };
 __device__ __forceinline__ int box_for_half(int n) {
-    return n <= 16 ? 0 : (n + 15) / 16 - 1;
+    return n <= 8 ? 0 : (n + 7) / 8 - 1;
 }
 __device__ __forceinline__ int box_half_rows(int box) {
-    return 16 * (box + 1);
+    return 8 * (box + 1);
 }
 
 struct TileInfo {
@@ -175,7 +181,9 @@ __device__ __forceinline__ void pair_sync(int pi) {
         case 0: named_barrier_sync<1>(64); break;
         case 1: named_barrier_sync<2>(64); break;
         case 2: named_barrier_sync<3>(64); break;
-        default: named_barrier_sync<4>(64); break;
+        case 3: named_barrier_sync<4>(64); break;
+        case 4: named_barrier_sync<5>(64); break;
+        default: named_barrier_sync<6>(64); break;
     }
 }
 
@@ -189,10 +197,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (sbase - raw);
-    __nv_bfloat16* xpose = reinterpret_cast<__nv_bfloat16*>(gbase + S * C::STAGE_BYTES);   // [8 warps][32][34]
-    float* pamax = reinterpret_cast<float*>(gbase + S * C::STAGE_BYTES + kEpiWarps * kXposeBytes);   // [4 pairs][2][32]
-    volatile int* pair_ok = reinterpret_cast<volatile int*>(pamax + (kEpiWarps / 2) * 2 * 32);   // [4 pairs][2 warps]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S * C::STAGE_BYTES + C::EPI_BYTES);
+    const uint32_t sfbase = sbase + S * C::STAGE_BYTES;                  // [S][SF_STAGE] scales
+    uint8_t* epi_base = gbase + S * (C::STAGE_BYTES + C::SF_STAGE);
+    __nv_bfloat16* xch = reinterpret_cast<__nv_bfloat16*>(epi_base);    // [6 pairs][2][32][kXchLd]
+    volatile int* pair_ok = reinterpret_cast<volatile int*>(epi_base + C::XCH_BYTES);   // [6 pairs][2 warps]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi_base + C::EPI_BYTES);
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (S + s); };
@@ -279,12 +288,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     TRACE_STAMP(c1);
                     const uint32_t sb = sbase + stage * C::STAGE_BYTES;
+                    const uint32_t ss = sfbase + stage * C::SF_STAGE;
                     if (!(starve && t == pair && kb == 0)) {
                         mbar_arrive_expect_tx_w(full(stage), bytes);
                         tma_load_2d_w(sb, &tmA, full(stage), kb * 128, a0);
                         tma_load_2d_w(sb + C::A_BYTES, tmBox, full(stage), kb * 128, brow);
-                        bulk_load_w(sb + C::SFA_OFF, sfa + kb * 512, 512, full(stage));
-                        bulk_load_w(sb + C::SFB_OFF, sfb + kb * 1024, C::SFB_BYTES, full(stage));
+                        bulk_load_w(ss, sfa + kb * 512, 512, full(stage));
+                        bulk_load_w(ss + 512, sfb + kb * 1024, C::SFB_BYTES, full(stage));
                         ++armed[ls];
                     }
                     TRACE_STAMP(c2);
@@ -371,13 +381,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     TRACE_STAMP(c1);
                     tc_fence_after();
                     const uint32_t sb = sbase + stage * C::STAGE_BYTES;
+                    const uint32_t ss = sfbase + stage * C::SF_STAGE;
                     const uint32_t sfs = sf_base + (kiter & 1u) * C::SF_SET_COLS;
                     ++kiter;
                     // descriptors of the stage; a K step of 32 bytes adds 2 to the address field
                     const uint64_t adesc = desc_kmajor_sw128(sb), bdesc = desc_kmajor_sw128(sb + C::A_BYTES);
-                    tc_cp_sf_pair_w(sfs, desc_sf_block(sb + C::SFA_OFF));
-                    tc_cp_sf_pair_w(sfs + 4, desc_sf_block(sb + C::SFB_OFF));
-                    if (two_sfb) tc_cp_sf_pair_w(sfs + 8, desc_sf_block(sb + C::SFB_OFF + 512));
+                    tc_cp_sf_pair_w(sfs, desc_sf_block(ss));
+                    tc_cp_sf_pair_w(sfs + 4, desc_sf_block(ss + 512));
+                    if (two_sfb) tc_cp_sf_pair_w(sfs + 8, desc_sf_block(ss + 1024));
                     tc_mma_mx_pair_w(d, adesc, bdesc, idk[0], sfs, sfs + 4, kb != 0);
                     tc_mma_mx_pair_w(d, adesc + 2, bdesc + 2, idk[1], sfs, sfs + 4, 1u);
                     tc_mma_mx_pair_w(d, adesc + 4, bdesc + 4, idk[2], sfs, sfs + 4, 1u);
@@ -402,7 +413,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;                              // TMEM lane quarter of this warp
-        const int grp = warp >> 2;                           // chunk parity of this warp
+        const int grp = warp >> 2;                           // this warp takes chunks grp, grp + 3, ...
         const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
         const uint32_t leader_tempty0 = map_shared_rank(tempty(0), 0);
         int it = 0;
@@ -432,14 +443,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int nchunks = (ti.nvalid + 31) / 32;
             const int mrow = ti.cb * 256 + 128 * static_cast<int>(rank);
             if constexpr (LAYER == 1) {
-                // quarter q holds band q of this CTA's 128 rows: gate (q even) or up
-                // (q odd) of channels cbase + [0, 32), cbase = mrow / 2 + 32 (q / 2)
+                // Quarter q holds band q of this CTA's 128 rows: gate (q even) or up
+                // (q odd) of channels cbase + [0, 32), cbase = mrow / 2 + 32 (q / 2);
+                // thread `lane` has channel cbase + lane for the chunk's 32 tokens.
+                // The gate warp finishes tokens 0-15 of a chunk and the up warp tokens
+                // 16-31; each hands the other the half of its values that it needs.
                 const int pr = q >> 1, hs = q & 1, pi = warp >> 1;
-                __nv_bfloat16* G = xpose + (2 * pi) * 32 * kXposeLd;
-                __nv_bfloat16* U = G + 32 * kXposeLd;
-                float* pam = pamax + pi * 64;
+                __nv_bfloat16* XG = xch + (2 * pi) * kXchElems;     // gate of tokens 16-31, for the up warp
+                __nv_bfloat16* XU = XG + kXchElems;                 // up of tokens 0-15, for the gate warp
                 const int cbase = mrow / 2 + 32 * pr;
-                for (int j = grp; j < nchunks; j += 2) {
+                const int mine0 = 16 * hs;                          // first token of this warp's half
+                for (int j = grp; j < nchunks; j += kEpiGroups) {
                     float v[32];
                     tmem_ld32(tacc + 32 * j, v);
                     if (p.debug_flags & 2) {
@@ -448,68 +462,108 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         for (int n = 0; n < 32 && 32 * j + n < ti.nvalid; ++n)
                             zd[static_cast<size_t>(ti.row0 + 32 * j + n) * 2 * p.I + hs * p.I + cbase + lane] = v[n];
                     }
-                    // g and u enter SwiGLU rounded to BF16, so the exchange holds BF16
-                    __nv_bfloat16* mine = hs ? U : G;
+                    // g and u enter SwiGLU rounded to BF16, so the hand-over holds BF16
+                    __nv_bfloat16* give = hs ? XU : XG;
+                    const int give0 = 16 - mine0;
 #pragma unroll
-                    for (int n = 0; n < 32; ++n) mine[n * kXposeLd + lane] = __float2bfloat16_rn(v[n]);
+                    for (int i = 0; i < 16; i += 2)
+                        *reinterpret_cast<__nv_bfloat162*>(give + lane * kXchLd + i) =
+                            __floats2bfloat162_rn(v[give0 + i], v[give0 + i + 1]);
+                    // top-k weights of this half's 16 tokens, one per lane, broadcast below
+                    const int r16 = 32 * j + mine0 + (lane & 15);
+                    const float wl = r16 < ti.nvalid ? __ldg(p.wpool + ti.row0 + r16) : 0.f;
                     pair_sync(pi);
-                    // this thread: token 32 j + lane, channels cbase + 16 hs + [0, 16)
-                    const int rloc = 32 * j + lane;
-                    const bool valid = rloc < ti.nvalid;
-                    const int row = ti.row0 + rloc;
-                    const float wv = valid ? __ldg(p.wpool + row) : 0.f;
+                    const __nv_bfloat16* take = hs ? XG : XU;
                     float h[16];
-                    float amax = 0.f;
 #pragma unroll
                     for (int i = 0; i < 16; i += 2) {
-                        const float2 g2 = __bfloat1622float2(
-                            *reinterpret_cast<const __nv_bfloat162*>(G + lane * kXposeLd + 16 * hs + i));
-                        const float2 u2 = __bfloat1622float2(
-                            *reinterpret_cast<const __nv_bfloat162*>(U + lane * kXposeLd + 16 * hs + i));
-                        h[i] = (g2.x / (1.0f + expf(-g2.x))) * u2.x * wv;
-                        h[i + 1] = (g2.y / (1.0f + expf(-g2.y))) * u2.y * wv;
-                        amax = fmaxf(amax, fmaxf(fabsf(h[i]), fabsf(h[i + 1])));
+                        const float2 o = __bfloat1622float2(
+                            *reinterpret_cast<const __nv_bfloat162*>(take + lane * kXchLd + i));
+                        const float m0 = bf16_round(v[mine0 + i]), m1 = bf16_round(v[mine0 + i + 1]);
+                        const float g0 = hs ? o.x : m0, u0 = hs ? m0 : o.x;
+                        const float g1 = hs ? o.y : m1, u1 = hs ? m1 : o.y;
+                        h[i] = silu(g0) * u0 * __shfl_sync(0xffffffffu, wl, i);
+                        h[i + 1] = silu(g1) * u1 * __shfl_sync(0xffffffffu, wl, i + 1);
                     }
-                    pam[hs * 32 + lane] = amax;
-                    pair_sync(pi);
-                    amax = fmaxf(amax, pam[(hs ^ 1) * 32 + lane]);
-                    const int ex = requant_exponent(amax);
-                    const float s = exp2_neg(ex);
-                    uint32_t pk[4];
+                    // Per token: amax over the 32 channels of the group (the warp's lanes).
+                    // A halving exchange: after the shuffle across lane bit b, a lane keeps
+                    // the maxima of half of its tokens, so 8 + 4 + 2 + 1 + 1 shuffles leave
+                    // lanes 2 i and 2 i + 1 with the amax of token i.
+                    float m8[8], m4[4], m2[2];
+                    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        pk[i] = e4m3x2(h[4 * i] * s, h[4 * i + 1] * s) | (e4m3x2(h[4 * i + 2] * s, h[4 * i + 3] * s) << 16);
-                    if (valid) {
-                        *reinterpret_cast<uint4*>(p.hpool + static_cast<size_t>(row) * p.I + cbase + 16 * hs) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        if (hs == 0) {
-                            // the L2 B-operand scale of this row and 32-channel group
-                            const int kb2 = cbase / 128, byte = (cbase % 128) / 32;
-                            const size_t wd = ((static_cast<size_t>(ti.tile_idx) * (p.I / 128) + kb2) * 2 + (rloc >> 7)) * 128 +
-                                              (rloc & 31) * 4 + ((rloc & 127) >> 5);
-                            p.hpool_sf[wd * 4 + byte] = static_cast<uint8_t>(ex + 127);
-                        }
+                    for (int k = 0; k < 8; ++k) {
+                        const float lo = fabsf(h[k]), hi = fabsf(h[k + 8]);
+                        m8[k] = fmaxf(b4 ? hi : lo, __shfl_xor_sync(0xffffffffu, b4 ? lo : hi, 16));
                     }
-                    pair_sync(pi);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        m4[k] = fmaxf(b3 ? m8[k + 4] : m8[k], __shfl_xor_sync(0xffffffffu, b3 ? m8[k] : m8[k + 4], 8));
+#pragma unroll
+                    for (int k = 0; k < 2; ++k)
+                        m2[k] = fmaxf(b2 ? m4[k + 2] : m4[k], __shfl_xor_sync(0xffffffffu, b2 ? m4[k] : m4[k + 2], 4));
+                    float m1 = fmaxf(b1 ? m2[1] : m2[0], __shfl_xor_sync(0xffffffffu, b1 ? m2[0] : m2[1], 2));
+                    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+                    const int my_ex = requant_exponent(m1);        // of token lane / 2
+                    const float my_s = exp2_neg(my_ex);
+                    // codes of channel `lane` for this half's 16 tokens, staged as
+                    // [token][32 channels] so that each lane then stores 16 bytes of a
+                    // row; the staging reuses the hand-over buffer this warp has read
+                    // (its partner writes it again only after the next pair barrier)
+                    __syncwarp();
+                    uint8_t* stg = reinterpret_cast<uint8_t*>(const_cast<__nv_bfloat16*>(take));
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        const uint32_t c2 = e4m3x2(h[i] * __shfl_sync(0xffffffffu, my_s, 2 * i),
+                                                   h[i + 1] * __shfl_sync(0xffffffffu, my_s, 2 * i + 2));
+                        stg[i * 32 + lane] = static_cast<uint8_t>(c2);
+                        stg[(i + 1) * 32 + lane] = static_cast<uint8_t>(c2 >> 8);
+                    }
+                    __syncwarp();
+                    // lane: token mine0 + lane / 2, channels cbase + 16 (lane & 1) + [0, 16)
+                    const int rc = 32 * j + mine0 + (lane >> 1);
+                    const uint4 cv = *reinterpret_cast<const uint4*>(stg + lane * 16);
+                    if (rc < ti.nvalid)
+                        *reinterpret_cast<uint4*>(p.hpool + static_cast<size_t>(ti.row0 + rc) * p.I + cbase +
+                                                  16 * (lane & 1)) = cv;
+                    // the L2 B-operand scale of this token and this 32-channel group
+                    if ((lane & 1) == 0 && rc < ti.nvalid) {
+                        const int kb2 = cbase / 128, byte = (cbase % 128) / 32;
+                        const size_t wd = ((static_cast<size_t>(ti.tile_idx) * (p.I / 128) + kb2) * 2 + (rc >> 7)) * 128 +
+                                          (rc & 31) * 4 + ((rc & 127) >> 5);
+                        p.hpool_sf[wd * 4 + byte] = static_cast<uint8_t>(my_ex + 127);
+                    }
+                    __syncwarp();                                   // the staging is reused by the next chunk
+                    pair_sync(pi);                                  // the buffers are free for the next chunk
                 }
             } else if (mrow < p.H) {
-                __nv_bfloat16* tb = xpose + warp * 32 * kXposeLd;
+                // thread `lane` has output channel cbase + lane for the chunk's 32 tokens;
+                // 16 tokens at a time are staged as BF16 [token][32 channels] (in this
+                // warp's share of the exchange buffers, unused by this layer) so that
+                // each lane stores 32 contiguous bytes of a row
                 const int cbase = mrow + 32 * q;
-                for (int j = grp; j < nchunks; j += 2) {
+                uint16_t* stg = reinterpret_cast<uint16_t*>(xch) + warp * kXchElems;
+                for (int j = grp; j < nchunks; j += kEpiGroups) {
                     float v[32];
                     tmem_ld32(tacc + 32 * j, v);
 #pragma unroll
-                    for (int n = 0; n < 32; ++n) tb[n * kXposeLd + lane] = __float2bfloat16_rn(v[n]);
-                    __syncwarp();
-                    const int rloc = 32 * j + lane;
-                    uint32_t pk[16];
+                    for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) pk[i] = *reinterpret_cast<const uint32_t*>(tb + lane * kXposeLd + 2 * i);
-                    __syncwarp();
-                    if (rloc < ti.nvalid) {
-                        uint4* dst = reinterpret_cast<uint4*>(p.ypool + static_cast<size_t>(ti.row0 + rloc) * p.H + cbase);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        for (int i = 0; i < 16; ++i) {
+                            const __nv_bfloat16 b = __float2bfloat16_rn(v[16 * hh + i]);
+                            stg[i * 32 + lane] = *reinterpret_cast<const uint16_t*>(&b);
+                        }
+                        __syncwarp();
+                        const int rc = 32 * j + 16 * hh + (lane >> 1);
+                        const uint4* src = reinterpret_cast<const uint4*>(stg + (lane >> 1) * 32 + 16 * (lane & 1));
+                        const uint4 y0 = src[0], y1 = src[1];
+                        if (rc < ti.nvalid) {
+                            uint4* dst = reinterpret_cast<uint4*>(p.ypool + static_cast<size_t>(ti.row0 + rc) * p.H + cbase +
+                                                                  16 * (lane & 1));
+                            dst[0] = y0;
+                            dst[1] = y1;
+                        }
+                        __syncwarp();
                     }
                 }
             }
@@ -576,8 +630,7 @@ cudaError_t launch_gemm(int layer, const CUtensorMap& tmA, const CUtensorMap* tm
     if (a.tile_n <= 32)
         return layer == 1 ? launch_one<1, 32, 32>(tmA, tmB, a, stream) : launch_one<2, 32, 32>(tmA, tmB, a, stream);
     if (a.tile_n <= 144)
-        return layer == 1 ? launch_one<1, kMaxTileN, 144>(tmA, tmB, a, stream)
-                          : launch_one<2, kMaxTileN, 144>(tmA, tmB, a, stream);
+        return layer == 1 ? launch_one<1, 144, 144>(tmA, tmB, a, stream) : launch_one<2, 144, 144>(tmA, tmB, a, stream);
     return layer == 1 ? launch_one<1, kMaxTileN, kMaxTileN>(tmA, tmB, a, stream)
                       : launch_one<2, kMaxTileN, kMaxTileN>(tmA, tmB, a, stream);
 }
