@@ -203,11 +203,13 @@ __global__ void __launch_bounds__(kChunk) layout_count_kernel(
     }
 }
 
+constexpr int kDispatchSplit = 4;   // warps per token row in the gather (divides 8)
+
 // ---------------------------------------------------------------------------
 // a3 part 2 + a4: slots, inverse map, pool weights, and the gather of token
 // rows and their scales into the expert-sorted pool.  Blocks [0, nb_tok) take
-// 8 tokens each (one warp per token); the remaining blocks fill the padding
-// rows of one expert each.
+// 8 / kDispatchSplit tokens each (kDispatchSplit warps per token); the
+// remaining blocks fill the padding rows of one expert each.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) dispatch_kernel(
     const uint8_t* __restrict__ x, const uint32_t* __restrict__ x_sf,
@@ -234,7 +236,10 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
         }
         return;
     }
-    const int t = blockIdx.x * 8 + warp;
+    // kDispatchSplit warps per token, each copying every kDispatchSplit-th
+    // 2 KB of the row (enough warps in flight for an HBM-bound copy)
+    const int part = warp % kDispatchSplit;
+    const int t = blockIdx.x * (8 / kDispatchSplit) + warp / kDispatchSplit;
     if (t >= T) return;
     const int Kb = H / 128;
     // lane j < k resolves entry (t, j)
@@ -251,10 +256,12 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
             const int rt = r % rows;
             // 128-row half of the tile, then word 4 l + c for row 32 c + l of that half
             word = (rt >> 7) * 128 + (rt & 31) * 4 + ((rt & 127) >> 5);
-            row2tk[slot] = i;
-            wpool[slot] = topk_w[i];
+            if (part == 0) {
+                row2tk[slot] = i;
+                wpool[slot] = topk_w[i];
+            }
         }
-        slots[i] = slot;
+        if (part == 0) slots[i] = slot;
     }
     // scales: word kb of the token's row goes to chunk `chunk`, K block kb
     for (int j = 0; j < k; ++j) {
@@ -262,13 +269,13 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
         const int c = __shfl_sync(0xffffffffu, chunk, j);
         const int wd = __shfl_sync(0xffffffffu, word, j);
         if (s < 0) continue;
-        for (int kb = lane; kb < Kb; kb += 32)
+        for (int kb = lane + 32 * part; kb < Kb; kb += 32 * kDispatchSplit)
             xpool_sf[(static_cast<size_t>(c) * Kb + kb) * 256 + wd] = x_sf[static_cast<size_t>(t) * Kb + kb];
     }
     // token row: read once, write to each valid slot (16-byte vectors)
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
     const int nv = H / 16;
-    for (int base = 0; base < nv; base += 32 * 4) {
+    for (int base = 128 * part; base < nv; base += 128 * kDispatchSplit) {
         uint4 buf[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -305,7 +312,8 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
                                                           a.tile_rows, a.status);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    const int nb_tok = (a.T + 7) / 8;
+    const int tok_per_block = 8 / kDispatchSplit;
+    const int nb_tok = (a.T + tok_per_block - 1) / tok_per_block;
     dispatch_kernel<<<nb_tok + a.E, 256, 0, stream>>>(
         a.x, a.x_sf, a.topk_idx, a.topk_w, a.T, a.H, a.E, a.k, a.hist, a.rank,
         a.counts, a.offsets, a.tiles, a.tile_rows, a.tile_expert, a.slots, a.row2tk, a.wpool, a.slack,
@@ -329,15 +337,24 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const int s = s_slot[j];
-            if (s < 0) continue;
-            const uint4 q = __ldg(reinterpret_cast<const uint4*>(ypool + static_cast<size_t>(s) * H) + v);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            // up to 8 slot rows in flight at once, then summed in j order
+            uint4 q[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] += __uint_as_float(w[i] << 16);
-                acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+            for (int jj = 0; jj < 8; ++jj) {
+                const int s = j0 + jj < k ? s_slot[j0 + jj] : -1;
+                q[jj] = s >= 0 ? __ldg(reinterpret_cast<const uint4*>(ypool + static_cast<size_t>(s) * H) + v)
+                               : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                if (j0 + jj >= k || s_slot[j0 + jj] < 0) continue;
+                const uint32_t w[4] = {q[jj].x, q[jj].y, q[jj].z, q[jj].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] += __uint_as_float(w[i] << 16);
+                    acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+                }
             }
         }
         uint32_t o[4];
