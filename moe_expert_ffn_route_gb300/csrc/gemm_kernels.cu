@@ -238,6 +238,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     cluster_sync();                                      // both CTAs' barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();                                          // the previous kernel's tables and pools are written
+    pdl_launch_dependents();
 
     const int npairs = gridDim.x >> 1, pair = blockIdx.x >> 1;
     const int ncb = LAYER == 1 ? p.I / 128 : (p.H + 255) / 256;   // 256-row weight tiles (pairs) per expert
@@ -605,6 +607,11 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap* tmB, co
     cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_pdl
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1) {
         (void)cudaGetLastError();

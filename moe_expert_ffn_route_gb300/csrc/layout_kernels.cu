@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(kChunk) layout_count_kernel(
     __shared__ int s_last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < 32 * E; i += kChunk) s_wcnt[i] = 0;
+    pdl_wait();
+    pdl_launch_dependents();
     __syncthreads();
 
     const int i = blockIdx.x * kChunk + tid;
@@ -221,6 +223,8 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
     float* __restrict__ wpool, int* __restrict__ slack, uint8_t* __restrict__ xpool,
     uint32_t* __restrict__ xpool_sf, int nb_tok) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_wait();
+    pdl_launch_dependents();
     if (static_cast<int>(blockIdx.x) >= nb_tok) {
         // padding rows, slack and token-tile owner of expert e
         const int e = blockIdx.x - nb_tok;
@@ -307,18 +311,15 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
         if (err != cudaSuccess) return err;
         attr_done = true;
     }
-    layout_count_kernel<<<nchunks, kChunk, smem, stream>>>(a.topk_idx, N, a.E, a.tile_n, a.hist,
-                                                          a.rank, a.counts, a.offsets, a.tiles,
-                                                          a.tile_rows, a.status);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(layout_count_kernel, dim3(nchunks), dim3(kChunk), smem, stream, a.topk_idx, N,
+                                 a.E, a.tile_n, a.hist, a.rank, a.counts, a.offsets, a.tiles, a.tile_rows,
+                                 a.status);
     if (err != cudaSuccess) return err;
     const int tok_per_block = 8 / kDispatchSplit;
     const int nb_tok = (a.T + tok_per_block - 1) / tok_per_block;
-    dispatch_kernel<<<nb_tok + a.E, 256, 0, stream>>>(
-        a.x, a.x_sf, a.topk_idx, a.topk_w, a.T, a.H, a.E, a.k, a.hist, a.rank,
-        a.counts, a.offsets, a.tiles, a.tile_rows, a.tile_expert, a.slots, a.row2tk, a.wpool, a.slack,
-        a.xpool, a.xpool_sf, nb_tok);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_kernel, dim3(nb_tok + a.E), dim3(256), 0, stream, a.x, a.x_sf, a.topk_idx,
+                      a.topk_w, a.T, a.H, a.E, a.k, a.hist, a.rank, a.counts, a.offsets, a.tiles, a.tile_rows,
+                      a.tile_expert, a.slots, a.row2tk, a.wpool, a.slack, a.xpool, a.xpool_sf, nb_tok);
 }
 
 // ---------------------------------------------------------------------------
@@ -330,6 +331,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
                                                       uint16_t* __restrict__ y) {
     __shared__ int s_slot[32];
     const int t = blockIdx.x;
+    pdl_wait();
+    pdl_launch_dependents();
     if (threadIdx.x < k) s_slot[threadIdx.x] = slots[static_cast<size_t>(t) * k + threadIdx.x];
     __syncthreads();
     const int nv = H / 8;
@@ -370,8 +373,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
 cudaError_t launch_combine(const uint16_t* ypool, const int* slots, int T, int H, int k,
                            uint16_t* y, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    combine_kernel<<<T, 128, 0, stream>>>(ypool, slots, H, k, y);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(T), dim3(128), 0, stream, ypool, slots, H, k, y);
 }
 
 // ---------------------------------------------------------------------------
