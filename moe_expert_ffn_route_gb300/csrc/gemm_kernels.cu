@@ -460,17 +460,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tmem_ld32(tacc + 32 * j, v);
                     if (p.debug_flags & 2) {
                         // test hook: raw FP32 accumulators, [P_max][gate I | up I] floats
+                        // (unrolled: a runtime index into v would move v to local memory)
                         float* zd = reinterpret_cast<float*>(p.ypool);
-                        for (int n = 0; n < 32 && 32 * j + n < ti.nvalid; ++n)
-                            zd[static_cast<size_t>(ti.row0 + 32 * j + n) * 2 * p.I + hs * p.I + cbase + lane] = v[n];
+#pragma unroll
+                        for (int n = 0; n < 32; ++n)
+                            if (32 * j + n < ti.nvalid)
+                                zd[static_cast<size_t>(ti.row0 + 32 * j + n) * 2 * p.I + hs * p.I + cbase + lane] = v[n];
+                    }
+                    // this warp's half and the half it hands over, selected with constant
+                    // indices so that v stays in registers
+                    float mine[16], other[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        mine[i] = hs ? v[16 + i] : v[i];
+                        other[i] = hs ? v[i] : v[16 + i];
                     }
                     // g and u enter SwiGLU rounded to BF16, so the hand-over holds BF16
                     __nv_bfloat16* give = hs ? XU : XG;
-                    const int give0 = 16 - mine0;
 #pragma unroll
                     for (int i = 0; i < 16; i += 2)
                         *reinterpret_cast<__nv_bfloat162*>(give + lane * kXchLd + i) =
-                            __floats2bfloat162_rn(v[give0 + i], v[give0 + i + 1]);
+                            __floats2bfloat162_rn(other[i], other[i + 1]);
                     // top-k weights of this half's 16 tokens, one per lane, broadcast below
                     const int r16 = 32 * j + mine0 + (lane & 15);
                     const float wl = r16 < ti.nvalid ? __ldg(p.wpool + ti.row0 + r16) : 0.f;
@@ -481,7 +491,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     for (int i = 0; i < 16; i += 2) {
                         const float2 o = __bfloat1622float2(
                             *reinterpret_cast<const __nv_bfloat162*>(take + lane * kXchLd + i));
-                        const float m0 = bf16_round(v[mine0 + i]), m1 = bf16_round(v[mine0 + i + 1]);
+                        const float m0 = bf16_round(mine[i]), m1 = bf16_round(mine[i + 1]);
                         const float g0 = hs ? o.x : m0, u0 = hs ? m0 : o.x;
                         const float g1 = hs ? o.y : m1, u1 = hs ? m1 : o.y;
                         h[i] = silu(g0) * u0 * __shfl_sync(0xffffffffu, wl, i);
