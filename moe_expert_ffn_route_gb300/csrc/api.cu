@@ -22,7 +22,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct WsLayout {
-    size_t status, counts, offsets, tiles, tile_rows, tile_expert, slots, rank, hist, row2tk, wpool, slack;
+    size_t status, counts, offsets, tiles, tile_rows, tile_rec, slots, rank, hist, row2tk, wpool, slack;
     size_t xpool, xpool_sf, hpool, hpool_sf, ypool, total;
     int64_t P_max, NT_max, nchunks;
 };
@@ -85,7 +85,7 @@ WsLayout ws_layout(const moeffn_problem& p) {
     L.offsets = take(4 * (E + 1));
     L.tiles = take(4 * (E + 1));
     L.tile_rows = take(4 * E);
-    L.tile_expert = take(4 * L.NT_max);
+    L.tile_rec = take(32 * L.NT_max);
     L.slots = take(4 * N);
     L.rank = take(4 * N);
     L.hist = take(4 * L.nchunks * E);
@@ -275,12 +275,12 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
     int* offsets = reinterpret_cast<int*>(w + L.offsets);
     int* tiles = reinterpret_cast<int*>(w + L.tiles);
     int* tile_rows = reinterpret_cast<int*>(w + L.tile_rows);
-    int* tile_expert = reinterpret_cast<int*>(w + L.tile_expert);
+    int* tile_rec = reinterpret_cast<int*>(w + L.tile_rec);
     int* slots = reinterpret_cast<int*>(w + L.slots);
 
     LayoutArgs la{x, x_sf, topk_idx, topk_w, T, H, E, k, tile_n,
                   reinterpret_cast<int*>(w + L.hist), reinterpret_cast<int*>(w + L.rank), counts, offsets,
-                  tiles, tile_rows, tile_expert, slots, reinterpret_cast<int*>(w + L.row2tk), reinterpret_cast<float*>(w + L.wpool),
+                  tiles, tile_rows, tile_rec, slots, reinterpret_cast<int*>(w + L.row2tk), reinterpret_cast<float*>(w + L.wpool),
                   reinterpret_cast<int*>(w + L.slack), w + L.xpool, reinterpret_cast<uint32_t*>(w + L.xpool_sf),
                   status};
     if (launch_layout(la, st) != cudaSuccess || !mark(1)) return MOEFFN_ERR_CUDA;
@@ -301,7 +301,7 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
     g.offsets = offsets;
     g.tiles = tiles;
     g.tile_rows = tile_rows;
-    g.tile_expert = tile_expert;
+    g.tile_rec = tile_rec;
     g.E = E;
     g.H = H;
     g.I = I;

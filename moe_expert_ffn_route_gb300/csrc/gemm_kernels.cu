@@ -157,20 +157,26 @@ struct TileInfo {
 // Work items run expert by expert; within an expert, weight-row tile by tile
 // and, inside one, token tile by token tile.  Expert e owns items
 // [tiles[e] * ncb, tiles[e + 1] * ncb), so item t / ncb is one of e's token
-// tiles and the token-tile owner table names e in one load.
-__device__ __forceinline__ TileInfo decode_tile(int t, int ncb, const GemmArgs& p) {
-    const int lo = __ldg(p.tile_expert + t / ncb);
+// tiles, whose 32-byte record holds what decoding item t needs.  The loops
+// load the next item's record while they work on the current item.
+struct TileRec {
+    int4 a;   // expert, its first token tile, its token tiles, rows per tile
+    int4 b;   // its first pool row, its rows
+};
+__device__ __forceinline__ TileRec load_rec(int t, int ncb, const GemmArgs& p) {
+    const int4* r = reinterpret_cast<const int4*>(p.tile_rec) + 2 * (t / ncb);
+    return TileRec{__ldg(r), __ldg(r + 1)};
+}
+__device__ __forceinline__ TileInfo decode_rec(int t, int ncb, const TileRec& r) {
     TileInfo ti;
-    const int t0 = __ldg(p.tiles + lo);
-    const int ntb = __ldg(p.tiles + lo + 1) - t0;
+    const int t0 = r.a.y, ntb = r.a.z, rows = r.a.w;
     const int local = t - t0 * ncb;
-    const int rows = __ldg(p.tile_rows + lo);
-    ti.e = lo;
+    ti.e = r.a.x;
     ti.cb = local / ntb;
     const int nb = local - ti.cb * ntb;
     ti.tile_idx = t0 + nb;
-    ti.row0 = __ldg(p.offsets + lo) + nb * rows;
-    ti.nvalid = min(rows, __ldg(p.counts + lo) - nb * rows);
+    ti.row0 = r.b.x + nb * rows;
+    ti.nvalid = min(rows, r.b.y - nb * rows);
     ti.ncols = rows;
     return ti;
 }
@@ -259,8 +265,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t armed[C::RING] = {};
             const bool starve = LAYER == 1 && (p.debug_flags & 1) && rank == 0 && ring == 0;
             bool ok = true;
-            for (int t = pair + ring * npairs; t < total && ok; t += 2 * npairs) {
-                const TileInfo ti = decode_tile(t, ncb, p);
+            const int t_first = pair + ring * npairs;
+            TileRec rec = t_first < total ? load_rec(t_first, ncb, p) : TileRec{};
+            for (int t = t_first; t < total && ok; t += 2 * npairs) {
+                const TileInfo ti = decode_rec(t, ncb, rec);
+                if (t + 2 * npairs < total) rec = load_rec(t + 2 * npairs, ncb, p);
                 const int mrow = ti.cb * 256 + 128 * static_cast<int>(rank);   // first weight row of this CTA
                 const bool mine_valid = mrow < a_rows;                          // false only for an L2 tail half
                 const int a0 = ti.e * a_rows + mrow;
@@ -355,8 +364,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t phase = 0, kiter = 0;
             bool ok = true;
             const uint32_t sf_base = tmem + C::SF_COL + static_cast<uint32_t>(ring * 2 * C::SF_SET_COLS);
-            for (int t = pair + ring * npairs; t < total && ok; t += 2 * npairs, ++it) {
-                const TileInfo ti = decode_tile(t, ncb, p);
+            const int t_first = pair + ring * npairs;
+            TileRec rec = t_first < total ? load_rec(t_first, ncb, p) : TileRec{};
+            for (int t = t_first; t < total && ok; t += 2 * npairs, ++it) {
+                const TileInfo ti = decode_rec(t, ncb, rec);
+                if (t + 2 * npairs < total) rec = load_rec(t + 2 * npairs, ncb, p);
                 const uint32_t idesc_n = IDESC | (static_cast<uint32_t>(ti.ncols >> 3) << 17);
                 const bool two_sfb = ti.ncols > 128;
                 const int tord = 2 * it + ring;                // ordinal of this tile in the pair's sequence
@@ -419,8 +431,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
         const uint32_t leader_tempty0 = map_shared_rank(tempty(0), 0);
         int it = 0;
+        TileRec rec = pair < total ? load_rec(pair, ncb, p) : TileRec{};
         for (int t = pair; t < total; t += npairs, ++it) {
-            const TileInfo ti = decode_tile(t, ncb, p);
+            const TileInfo ti = decode_rec(t, ncb, rec);
+            if (t + npairs < total) rec = load_rec(t + npairs, ncb, p);
             const int as = it % ACC;
             const uint32_t ap = static_cast<uint32_t>(it / ACC) & 1u;
             unsigned long long e0 = 0, e1 = 0, e2 = 0;

@@ -21,7 +21,8 @@ struct LayoutArgs {
     int* offsets;   // [E+1]
     int* tiles;     // [E+1] first token tile of each expert
     int* tile_rows; // [E]   token rows per tile of each expert (multiple of 16)
-    int* tile_expert; // [NT_max] expert of each token tile
+    int* tile_rec;  // [NT_max][8] per token tile: expert, its first token tile, its token
+                    // tiles, rows per tile, its pool offset, its rows, 0, 0
     int* slots;     // [T*k]
     int* row2tk;    // [P_max]
     float* wpool;   // [P_max]
@@ -50,7 +51,7 @@ struct GemmArgs {
     const int* offsets;
     const int* tiles;
     const int* tile_rows;
-    const int* tile_expert;  // expert of each token tile
+    const int* tile_rec;     // per token tile: its expert's tile record (LayoutArgs)
     int E;
     int H, I;
     const uint8_t* sfa;     // prepared weight scales (per 128-row block, per K block)

@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
     const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int T, int H, int E,
     int k, const int* __restrict__ hist, const int* __restrict__ rank,
     const int* __restrict__ counts, const int* __restrict__ offsets,
-    const int* __restrict__ tiles, const int* __restrict__ tile_rows, int* __restrict__ tile_expert,
+    const int* __restrict__ tiles, const int* __restrict__ tile_rows, int* __restrict__ tile_rec,
     int* __restrict__ slots, int* __restrict__ row2tk,
     float* __restrict__ wpool, int* __restrict__ slack, uint8_t* __restrict__ xpool,
     uint32_t* __restrict__ xpool_sf, int nb_tok) {
@@ -226,10 +226,15 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
     pdl_wait();
     pdl_launch_dependents();
     if (static_cast<int>(blockIdx.x) >= nb_tok) {
-        // padding rows, slack and token-tile owner of expert e
+        // padding rows, slack and the tile records of expert e
         const int e = blockIdx.x - nb_tok;
         const int n = counts[e], beg = offsets[e], end = offsets[e + 1];
-        for (int tt = tiles[e] + threadIdx.x; tt < tiles[e + 1]; tt += blockDim.x) tile_expert[tt] = e;
+        const int t0 = tiles[e], t1 = tiles[e + 1];
+        for (int tt = t0 + threadIdx.x; tt < t1; tt += blockDim.x) {
+            int4* rec = reinterpret_cast<int4*>(tile_rec) + 2 * tt;
+            rec[0] = make_int4(e, t0, t1 - t0, tile_rows[e]);
+            rec[1] = make_int4(beg, n, 0, 0);
+        }
         for (int r = beg + n + threadIdx.x; r < end; r += blockDim.x) {
             row2tk[r] = -1;
             wpool[r] = 0.f;
@@ -319,7 +324,7 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
     const int nb_tok = (a.T + tok_per_block - 1) / tok_per_block;
     return launch_pdl(dispatch_kernel, dim3(nb_tok + a.E), dim3(256), 0, stream, a.x, a.x_sf, a.topk_idx,
                       a.topk_w, a.T, a.H, a.E, a.k, a.hist, a.rank, a.counts, a.offsets, a.tiles, a.tile_rows,
-                      a.tile_expert, a.slots, a.row2tk, a.wpool, a.slack, a.xpool, a.xpool_sf, nb_tok);
+                      a.tile_rec, a.slots, a.row2tk, a.wpool, a.slack, a.xpool, a.xpool_sf, nb_tok);
 }
 
 // ---------------------------------------------------------------------------
