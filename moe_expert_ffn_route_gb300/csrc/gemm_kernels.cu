@@ -112,8 +112,7 @@ struct GemmCfg {
     // then one 512-byte chunk of token scales per 128 tile rows
     static constexpr int SFB_BYTES = BN <= 128 ? 512 : 1024;
     static constexpr int SF_STAGE = 512 + SFB_BYTES;
-    // per gate/up warp pair two BF16 exchange buffers (L2: one staging buffer per
-    // epilogue warp in the same bytes); per pair warp a vote word
+    // per gate/up warp pair two BF16 exchange buffers (L1); per pair warp a vote word
     static constexpr int XCH_BYTES = (kEpiWarps / 2) * 2 * kXchElems * 2;
     static constexpr int EPI_BYTES = XCH_BYTES + 4 * kEpiWarps;
     static constexpr int FIXED = 1024 + EPI_BYTES + 256;
@@ -568,28 +567,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // warp's share of the exchange buffers, unused by this layer) so that
                 // each lane stores 32 contiguous bytes of a row
                 const int cbase = mrow + 32 * q;
-                uint16_t* stg = reinterpret_cast<uint16_t*>(xch) + warp * kXchElems;
+                // lanes 2m and 2m + 1 swap halves: the even lane then holds channels
+                // (2m, 2m + 1) of tokens 0-15, the odd lane of tokens 16-31, and each
+                // stores one BF16 pair per token (the warp writes 64 contiguous bytes)
+                const bool odd = lane & 1;
+                const int c2 = cbase + (lane & ~1);
                 for (int j = grp; j < nchunks; j += kEpiGroups) {
                     float v[32];
                     tmem_ld32(tacc + 32 * j, v);
+                    const int nrows = min(32, ti.nvalid - 32 * j);
+                    uint16_t* dst = p.ypool + static_cast<size_t>(ti.row0 + 32 * j + (odd ? 16 : 0)) * p.H + c2;
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const __nv_bfloat16 b = __float2bfloat16_rn(v[16 * hh + i]);
-                            stg[i * 32 + lane] = *reinterpret_cast<const uint16_t*>(&b);
-                        }
-                        __syncwarp();
-                        const int rc = 32 * j + 16 * hh + (lane >> 1);
-                        const uint4* src = reinterpret_cast<const uint4*>(stg + (lane >> 1) * 32 + 16 * (lane & 1));
-                        const uint4 y0 = src[0], y1 = src[1];
-                        if (rc < ti.nvalid) {
-                            uint4* dst = reinterpret_cast<uint4*>(p.ypool + static_cast<size_t>(ti.row0 + rc) * p.H + cbase +
-                                                                  16 * (lane & 1));
-                            dst[0] = y0;
-                            dst[1] = y1;
-                        }
-                        __syncwarp();
+                    for (int n = 0; n < 16; ++n) {
+                        // even lane sends its token 16 + n, odd lane its token n
+                        const float send = odd ? v[n] : v[16 + n];
+                        const float got = __shfl_xor_sync(0xffffffffu, send, 1);
+                        const float keep = odd ? v[16 + n] : v[n];
+                        const __nv_bfloat162 b2 = odd ? __floats2bfloat162_rn(got, keep) : __floats2bfloat162_rn(keep, got);
+                        if (n + (odd ? 16 : 0) < nrows)
+                            *reinterpret_cast<__nv_bfloat162*>(dst + static_cast<size_t>(n) * p.H) = b2;
                     }
                 }
             }
