@@ -591,7 +591,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(leader_tempty0 + 8u * as);
+            // relaxed: what the MMA warp must not overtake are this warp's TMEM loads,
+            // complete (tcgen05.wait::ld) and fenced above; the rows stored to global
+            // memory are not read by that warp, and a release would wait for them
+            if (lane == 0) mbar_arrive_remote_relaxed(leader_tempty0 + 8u * as);
             TRACE_STAMP(e2);
             if (warp == 0 && lane == 0) TRACE_PUT(2, it, e0, e1, e2);
         }
