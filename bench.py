@@ -143,9 +143,15 @@ def traffic_from_profile(kernel_src_hash: str, workload: str, units_scale: float
 
 
 def kernel_hash() -> str:
+    """sha256 of the GEMM kernel's source with `//` comments, trailing spaces
+    and blank lines removed: a change of comments keeps a profile valid."""
     h = hashlib.sha256()
     for f in ("gemm_kernels.cu", "common.cuh"):
-        h.update(open(os.path.join(ROOT, "moe_expert_ffn_route_gb300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "moe_expert_ffn_route_gb300", "csrc", f)).read()
+        for line in text.splitlines():
+            code = re.sub(r"//.*$", "", line).rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()
 
 

@@ -23,18 +23,21 @@
 //    full token-tile scales in its tensor memory.  A stage therefore holds
 //    one 128-row weight tile and half a token tile per SM.
 //  - A block-scaled MMA (K = 32) occupies an SM's tensor core for
-//    max(48, N/2) cycles, but one thread issues one only every ~100-130
-//    cycles (with its scale copies), so token tiles are wide and two warps
-//    issue MMAs: each expert's rows are split into equal tiles of a multiple
-//    of 16 rows, at most BN (224, or 32 for decode-sized batches, where the
-//    narrow stages allow 10 in flight).
-//  - Persistent: pair p takes tiles p, p + P, ...; the even and the odd ones
-//    go to two MMA warps, each with its own ring of stages, every stage with
-//    its own TMA warp; eight warps drain TMEM.  Tiles use accumulator regions
-//    in turn: two of 224 columns, or three of 144 when no tile is wider.
+//    max(48, N/2) cycles, so token tiles are wide: each expert's rows are
+//    split into equal tiles of a multiple of 16 rows, at most 144 (most
+//    experts), 224 (more than ~272 rows per expert) or 32 (decode-sized
+//    batches, where narrow stages allow 10 in flight).
+//  - Persistent: pair p takes work items p, p + P, ...; the even and the odd
+//    ones go to two MMA warps, each with its own ring of stages (4 for tiles
+//    of at most 144 rows) fed by its own TMA warp; twelve warps drain TMEM.
+//    Items use accumulator regions in turn (three of 144 columns, two of
+//    224 or four of 32), so an MMA warp rarely waits for the epilogue.
+//  - The MMA and TMA warps issue from all 32 lanes through elect.sync; the
+//    forward's kernels use programmatic dependent launch.
 //  - For L1 a CTA's 128 weight rows are gate and up of 64 channels in bands
 //    of 32; the warps draining the gate and the up band of a channel group
-//    pair up through shared memory for SwiGLU and requantisation.
+//    each finish half of a chunk's tokens, exchanging the other half through
+//    shared memory, for SwiGLU and requantisation.
 //  - Scale factors of a token tile are stored per tile in tensor-memory copy
 //    order (two 512-byte chunks per 128-wide K block).
 #include "common.cuh"
