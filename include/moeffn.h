@@ -70,9 +70,9 @@ typedef void* moeffn_stream;
  *   "Activation clamp"); <= 0 disables it.  Values > 0 are not built yet and
  *   return MOEFFN_ERR_UNSUPPORTED.
  * fast_math: 0 = expf and a correctly rounded quotient in SiLU (Markstein's
- *   division method, checked bit for bit against IEEE division on the GPU over
- *   the SiLU inputs).  Non-zero is not built yet
- *   and returns MOEFFN_ERR_UNSUPPORTED.
+ *   division method, checked bit for bit against IEEE division on the GPU for
+ *   every BF16 input).  Non-zero is not built yet and returns
+ *   MOEFFN_ERR_UNSUPPORTED.
  * tile_n: most token rows per grouped-GEMM tile, a multiple of 16 in
  *   [32, 224]; 0 = 32 when T*k/E <= 32, 144 when T*k/E <= 272, else 224.
  *   Each expert's rows are split into ceil(n_e/tile_n) equal tiles rounded
