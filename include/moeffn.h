@@ -67,11 +67,13 @@ typedef void* moeffn_stream;
  *   UE8M0 packing granularity, as the MegaMoE host checks require);
  *   1 <= num_experts E <= 1024; 1 <= topk k <= min(E, 32).
  * act_clamp: optional activation clamp of the L1 epilogue (MegaMoE notes,
- *   "Activation clamp"); <= 0 disables it.  Values > 0 are not built yet and
- *   return MOEFFN_ERR_UNSUPPORTED.
+ *   "Activation clamp"; the pages' default threshold is 10): for c > 0 the
+ *   BF16 gate value is clamped to <= c and the up value to [-c, c] before
+ *   SwiGLU.  <= 0 disables it (the configs); NaN -> MOEFFN_ERR_INVALID_ARG.
  * fast_math: 0 = expf and a correctly rounded quotient in SiLU (Markstein's
  *   division method, checked bit for bit against IEEE division on the GPU for
- *   every BF16 input).  Non-zero is not built yet and returns
+ *   every BF16 input); 1 = approximate exponential and reciprocal (__expf,
+ *   __fdividef), the pages' fast-math switch.  Other values return
  *   MOEFFN_ERR_UNSUPPORTED.
  * tile_n: most token rows per grouped-GEMM tile, a multiple of 16 in
  *   [32, 224]; 0 = 32 when T*k/E <= 32, 144 when T*k/E <= 272, else 224.

@@ -43,7 +43,8 @@ moeffn_status check_problem(const moeffn_problem* p) {
     if (p->debug_flags & ~(MOEFFN_DEBUG_STARVE_L1 | MOEFFN_DEBUG_DUMP_L1_ACC)) return MOEFFN_ERR_INVALID_ARG;
     if ((p->debug_flags & MOEFFN_DEBUG_DUMP_L1_ACC) && 4 * p->intermediate > p->hidden)
         return MOEFFN_ERR_UNSUPPORTED;
-    if (p->act_clamp > 0.f || p->fast_math != 0) return MOEFFN_ERR_UNSUPPORTED;
+    if (!(p->act_clamp <= 0.f || p->act_clamp > 0.f)) return MOEFFN_ERR_INVALID_ARG;   // NaN
+    if (p->fast_math != 0 && p->fast_math != 1) return MOEFFN_ERR_UNSUPPORTED;
     // sizes used in 32-bit index arithmetic on the device
     const int64_t N = static_cast<int64_t>(p->num_tokens) * p->topk;
     if (N > (int64_t(1) << 26)) return MOEFFN_ERR_INVALID_ARG;
@@ -312,6 +313,8 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
     g.status = status;
     g.timeout_ns = static_cast<uint64_t>(p->wait_timeout_us ? p->wait_timeout_us : 2000000) * 1000ull;
     g.debug_flags = p->debug_flags;
+    g.act_clamp = p->act_clamp > 0.f ? p->act_clamp : 0.f;
+    g.fast_math = p->fast_math;
     g.num_sms = num_sms;
     g.tile_n = tile_n;
 

@@ -471,6 +471,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 __nv_bfloat16* XU = XG + kXchElems;                 // up of tokens 0-15, for the gate warp
                 const int cbase = mrow / 2 + 32 * pr;
                 const int mine0 = 16 * hs;                          // first token of this warp's half
+                const float clamp = p.act_clamp;
                 for (int j = grp; j < nchunks; j += kEpiGroups) {
                     float v[32];
                     tmem_ld32(tacc + 32 * j, v);
@@ -502,16 +503,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const float wl = r16 < ti.nvalid ? __ldg(p.wpool + ti.row0 + r16) : 0.f;
                     pair_sync(pi);
                     const __nv_bfloat16* take = hs ? XG : XU;
-                    float h[16];
+                    float g[16], u[16];
 #pragma unroll
                     for (int i = 0; i < 16; i += 2) {
                         const float2 o = __bfloat1622float2(
                             *reinterpret_cast<const __nv_bfloat162*>(take + lane * kXchLd + i));
                         const float m0 = bf16_round(mine[i]), m1 = bf16_round(mine[i + 1]);
-                        const float g0 = hs ? o.x : m0, u0 = hs ? m0 : o.x;
-                        const float g1 = hs ? o.y : m1, u1 = hs ? m1 : o.y;
-                        h[i] = silu(g0) * u0 * __shfl_sync(0xffffffffu, wl, i);
-                        h[i + 1] = silu(g1) * u1 * __shfl_sync(0xffffffffu, wl, i + 1);
+                        g[i] = hs ? o.x : m0;
+                        u[i] = hs ? m0 : o.x;
+                        g[i + 1] = hs ? o.y : m1;
+                        u[i + 1] = hs ? m1 : o.y;
+                    }
+                    if (clamp > 0.f) {
+                        // optional activation clamp (MegaMoE notes, "Activation clamp"):
+                        // the gate from above only, the up projection on both sides
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            g[i] = fminf(g[i], clamp);
+                            u[i] = fminf(fmaxf(u[i], -clamp), clamp);
+                        }
+                    }
+                    float h[16];
+                    if (p.fast_math) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) h[i] = silu_fast(g[i]) * u[i] * __shfl_sync(0xffffffffu, wl, i);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) h[i] = silu(g[i]) * u[i] * __shfl_sync(0xffffffffu, wl, i);
                     }
                     // Per token: amax over the 32 channels of the group (the warp's lanes).
                     // A halving exchange: after the shuffle across lane bit b, a lane keeps

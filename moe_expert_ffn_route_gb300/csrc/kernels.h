@@ -63,6 +63,8 @@ struct GemmArgs {
     DevStatus* status;
     uint64_t timeout_ns;
     int debug_flags;
+    float act_clamp;        // > 0: L1 epilogue clamps gate <= c and -c <= up <= c
+    int fast_math;          // 1: SiLU with approximate exp and reciprocal
     int num_sms;
     int tile_n;             // most token rows per tile (selects the stage layout)
 };

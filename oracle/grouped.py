@@ -74,8 +74,10 @@ def _e4m3_rne(v: np.ndarray) -> np.ndarray:
     return (pick | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
 
 
-def forward_grouped(inp: dict, idx: np.ndarray, w: np.ndarray, block: int = 128):
-    """Returns (y bf16 bits [T,H], q codes [T,k,I], qe exponents [T,k,I/32])."""
+def forward_grouped(inp: dict, idx: np.ndarray, w: np.ndarray, block: int = 128, clamp: float = 0.0):
+    """Returns (y bf16 bits [T,H], q codes [T,k,I], qe exponents [T,k,I/32]).
+    clamp > 0: the optional activation clamp of the L1 epilogue (MegaMoE notes,
+    "Activation clamp"): gate limited above, up on both sides, after the BF16 cast."""
     x, x_sf = inp["x"], inp["x_sf"]
     T, H = x.shape
     E, I2, _ = inp["w1"].shape
@@ -99,6 +101,9 @@ def forward_grouped(inp: dict, idx: np.ndarray, w: np.ndarray, block: int = 128)
         Wg, Wu = W1[rows[:, 0, :].reshape(-1)], W1[rows[:, 1, :].reshape(-1)]
         g = _bf16(X @ Wg.T)
         u = _bf16(X @ Wu.T)
+        if clamp > 0:
+            g = np.minimum(g, clamp)
+            u = np.clip(u, -clamp, clamp)
         Hm = g / (1.0 + np.exp(-g)) * u * w[tok, jj][:, None].astype(np.float64)
         grp = Hm.reshape(len(ent), I // 32, 32)
         amax = np.abs(grp).max(axis=-1)

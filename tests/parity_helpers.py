@@ -31,11 +31,12 @@ def dims(inp):
 class GpuRun:
     """One forward on the GPU; keeps the device tensors for inspection."""
 
-    def __init__(self, inp, idx, w, tile_n=0, debug_flags=0, wait_timeout_us=0, weights=None):
+    def __init__(self, inp, idx, w, tile_n=0, debug_flags=0, wait_timeout_us=0, weights=None,
+                 act_clamp=0.0, fast_math=0):
         T, H, I, E = dims(inp)
         k = idx.shape[1]
         self.prob = mb.problem(T, H, I, E, k, tile_n=tile_n, debug_flags=debug_flags,
-                               wait_timeout_us=wait_timeout_us)
+                               wait_timeout_us=wait_timeout_us, act_clamp=act_clamp, fast_math=fast_math)
         self.tile_n = mb.tile_n(self.prob)
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
         if weights is None:

@@ -52,8 +52,10 @@ def test_status_strings():
     (dict(tile_n=96), mb.OK),
     (dict(tile_n=192), mb.OK),
     (dict(tile_n=224), mb.OK),
-    (dict(act_clamp=10.0), mb.ERR_UNSUPPORTED),
-    (dict(fast_math=1), mb.ERR_UNSUPPORTED),
+    (dict(act_clamp=10.0), mb.OK),
+    (dict(act_clamp=float("nan")), mb.ERR_INVALID_ARG),
+    (dict(fast_math=1), mb.OK),
+    (dict(fast_math=2), mb.ERR_UNSUPPORTED),
     (dict(debug_flags=4), mb.ERR_INVALID_ARG),
     (dict(debug_flags=2, H=1024, I=512), mb.ERR_UNSUPPORTED),
     (dict(debug_flags=2, H=1024, I=256), mb.OK),

@@ -137,9 +137,9 @@ def _small(T=96, H=512, I=256, E=6, k=2, seed=31, empty=0.0, skew=False):
     return inp, idx, w
 
 
-def _check_full(inp, idx, w, run):
+def _check_full(inp, idx, w, run, clamp=0.0):
     T = inp["x"].shape[0]
-    ref = oracle.forward(inp, idx, w, want_codes=True)
+    ref = oracle.forward(inp, idx, w, want_codes=True, clamp=clamp)
     lay = oracle.layout(idx, run.E)
     tabs = run.tables()
     for key in ("counts", "offsets", "slots", "row2tk", "slack"):
@@ -159,6 +159,27 @@ def test_every_token_tile(tile_n):
     inp, idx, w = _small(T=200, E=5, k=2, skew=True)
     run = GpuRun(inp, idx, w, tile_n=tile_n)
     assert run.tile_n == tile_n and run.status()[0] == mb.OK
+    _check_full(inp, idx, w, run)
+
+
+@pytest.mark.parametrize("clamp", [10.0, 0.5])
+def test_activation_clamp(clamp):
+    # 10 is the pages' default threshold; 0.5 clamps a large share of gate and up values
+    inp, idx, w = _small(T=120, E=5, k=2, seed=41)
+    run = GpuRun(inp, idx, w, act_clamp=clamp)
+    assert run.status()[0] == mb.OK
+    _check_full(inp, idx, w, run, clamp=clamp)
+    if clamp < 1.0:
+        # the clamp is live: the clamped oracle and the plain one differ here
+        plain = oracle.forward(inp, idx, w)["y"]
+        assert not np.array_equal(run.y_bits(), plain)
+
+
+def test_fast_math_meets_the_same_bars():
+    # approximate exp and reciprocal in SiLU, against the exact oracle
+    inp, idx, w = _small(T=160, E=6, k=2, seed=43)
+    run = GpuRun(inp, idx, w, fast_math=1)
+    assert run.status()[0] == mb.OK
     _check_full(inp, idx, w, run)
 
 

@@ -240,6 +240,36 @@ def test_grouped_equals_direct():
         assert np.array_equal(d["y"], y)
 
 
+def test_activation_clamp_pins():
+    """The optional clamp (MegaMoE notes, "Activation clamp": gate limited above,
+    up on both sides): grouped and direct forms agree; a clamp above every value
+    changes nothing; a small clamp bounds every requantised activation."""
+    inp, idx, w = _tiny(T=30, H=256, I=128, E=3, k=2, seed=12, empty=0.0)
+    plain = oracle.forward(inp, idx, w, want_codes=True)
+    # no-op when the threshold exceeds every gate and up value
+    big = oracle.forward(inp, idx, w, want_codes=True, clamp=1e30)
+    assert np.array_equal(big["y"], plain["y"]) and np.array_equal(big["q"], plain["q"])
+    for c in (0.5, 2.0, 10.0):
+        d = oracle.forward(inp, idx, w, want_codes=True, clamp=c)
+        y, q, qe = forward_grouped(inp, idx, w, clamp=c)
+        assert np.array_equal(d["qe"], qe) and np.array_equal(d["q"], q) and np.array_equal(d["y"], y)
+    # with c = 0.5: |h| = |silu(g) u w| <= max(silu(c), -min silu) * c * w; the decoded E4M3
+    # value is within half a step (1/16 relative) of h
+    c = 0.5
+    d = oracle.forward(inp, idx, w, want_codes=True, clamp=c)
+    assert not np.array_equal(d["y"], plain["y"])        # the clamp is live on these inputs
+    hdec = _e4m3_table()[d["q"]] * np.ldexp(1.0, d["qe"].astype(np.int64))[..., None].repeat(32, -1).reshape(d["q"].shape)
+    bound = max(c / (1 + np.exp(-c)), 0.2785) * c * w[..., None] * (1 + 1 / 16)
+    assert np.all(np.abs(hdec) <= bound)
+    # and without the clamp the same inputs exceed that bound somewhere
+    hplain = _e4m3_table()[plain["q"]] * np.ldexp(1.0, plain["qe"].astype(np.int64))[..., None].repeat(32, -1).reshape(plain["q"].shape)
+    assert np.any(np.abs(hplain) > bound)
+
+
+def _e4m3_table():
+    return torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
 def _e2m1_to_torch(codes):
     """E2M1 code -> value via an E4M3 bit pattern (bias 1 -> bias 7) and torch."""
     c = codes.astype(np.int32)
