@@ -194,7 +194,11 @@ MOEFFN_API moeffn_status moeffn_route_topk(const float* logits, int32_t num_toke
  *   y          uint16 BF16 [T][H] out: sum over valid j of the BF16 L2 rows,
  *              accumulated in FP32 in j order, rounded to BF16 (RNE)
  * Errors: see the conventions above; workspace_bytes too small ->
- * WORKSPACE_TOO_SMALL.  T = 0 launches nothing. */
+ * WORKSPACE_TOO_SMALL.  T = 0 launches nothing.
+ * On `stream` the call only launches kernels (the host checks arguments and
+ * encodes tensor maps), so moeffn_route_topk and moeffn_forward can be
+ * captured in a CUDA graph; a replay recomputes from what the buffers hold
+ * then (tests/test_gpu_graph.py). */
 MOEFFN_API moeffn_status moeffn_forward(const moeffn_problem* problem,
                              const uint8_t* x, const uint32_t* x_sf,
                              const int64_t* topk_idx, const float* topk_w,
