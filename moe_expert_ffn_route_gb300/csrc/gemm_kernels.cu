@@ -674,10 +674,9 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap* tmB, co
 
 cudaError_t launch_gemm(int layer, const CUtensorMap& tmA, const CUtensorMap* tmB, const GemmArgs& a,
                         cudaStream_t stream) {
-    // stage layouts for tiles of at most 32 and kMaxTileN rows (a layout for
-    // 128-row tiles, with 8 narrower stages in flight, measured slower on
-    // 128-row tiles than the kMaxTileN layout's 6 stages); tiles of at most
-    // 144 rows get three accumulator regions instead of two
+    // three stage layouts: tiles of at most 32 rows (10 stages in flight, four
+    // accumulator regions), at most 144 rows (8 stages, three regions) and at
+    // most kMaxTileN rows (6 stages, two regions)
     if (a.tile_n <= 32)
         return layer == 1 ? launch_one<1, 32, 32>(tmA, tmB, a, stream) : launch_one<2, 32, 32>(tmA, tmB, a, stream);
     if (a.tile_n <= 144)
