@@ -298,10 +298,7 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
             return MOEFFN_ERR_CUDA;
 
     GemmArgs g{};
-    g.counts = counts;
-    g.offsets = offsets;
     g.tiles = tiles;
-    g.tile_rows = tile_rows;
     g.tile_rec = tile_rec;
     g.E = E;
     g.H = H;

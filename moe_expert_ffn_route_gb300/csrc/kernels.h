@@ -47,10 +47,7 @@ struct PrepareArgs {
 // One grouped GEMM launch (L1: Xpool x W1 with the SwiGLU/requant epilogue;
 // L2: Hpool x W2 with the BF16 epilogue).
 struct GemmArgs {
-    const int* counts;
-    const int* offsets;
-    const int* tiles;
-    const int* tile_rows;
+    const int* tiles;        // [E+1] first token tile of each expert (tiles[E]: all tiles)
     const int* tile_rec;     // per token tile: its expert's tile record (LayoutArgs)
     int E;
     int H, I;

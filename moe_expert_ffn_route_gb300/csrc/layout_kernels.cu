@@ -308,13 +308,11 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
     const int N = a.T * a.k;
     const int nchunks = (N + kChunk - 1) / kChunk;
     const size_t smem = static_cast<size_t>(32) * a.E * sizeof(int);
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t err = cudaFuncSetAttribute(layout_count_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               32 * 1024 * static_cast<int>(sizeof(int)));
+    if (smem > 48 * 1024) {
+        // per device and cheap: set on every launch that needs more than the default
+        cudaError_t err = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
         if (err != cudaSuccess) return err;
-        attr_done = true;
     }
     cudaError_t err = launch_pdl(layout_count_kernel, dim3(nchunks), dim3(kChunk), smem, stream, a.topk_idx, N,
                                  a.E, a.tile_n, a.hist, a.rank, a.counts, a.offsets, a.tiles, a.tile_rows,
