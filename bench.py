@@ -125,7 +125,90 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi -lms 20"}
+
+
+class NvmlSampler:
+    """The same record read through NVML every 2 ms by a thread while running
+    (nvidia-smi answers every ~20 ms, which leaves a timed region of a few ms
+    without a sample).  Reads only; raises OSError where NVML or the device's
+    handle is unavailable, and the caller falls back to ClockSampler."""
+
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+               ("sw_power_cap", 0x4))
+
+    def __init__(self, dev):
+        import ctypes
+        import torch
+        self.ct = ctypes
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError as e:
+            raise OSError(f"no NVML: {e}")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(dev)
+        bus = getattr(props, "pci_bus_id", None)
+        if bus is not None:
+            busid = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), bus, getattr(props, "pci_device_id", 0))
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(busid.encode(), ctypes.byref(self.h))
+        else:
+            n = ctypes.c_uint()
+            if self.lib.nvmlDeviceGetCount_v2(ctypes.byref(n)) != 0 or n.value != torch.cuda.device_count():
+                raise OSError("cannot match the CUDA device to an NVML device")
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(dev.index, ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError(f"no NVML handle ({rc})")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        if self.reasons_fn is None:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 else None
+        self.samples = []
+        self.stop = threading.Event()
+        if self._sample() is None:
+            raise OSError("NVML clock query failed")
+
+    def _sample(self):
+        ct = self.ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) != 0:   # 1: NVML_CLOCK_SM
+            return None
+        if self.reasons_fn(self.h, ct.byref(rs)) != 0:
+            return None
+        return float(clk.value), int(rs.value)
+
+    def _poll(self):
+        while not self.stop.is_set():
+            v = self._sample()
+            if v is not None:
+                self.samples.append(v)
+            self.stop.wait(0.002)
+
+    def __enter__(self):
+        self.samples = []
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self.stop.set()
+        self.thread.join(timeout=5)
+
+    def summary(self):
+        reasons = sorted({n for _, r in self.samples for n, bit in self.REASONS if r & bit})
+        sm = [c for c, _ in self.samples]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(sm), "source": "nvml, every 2 ms"}
+
+
+def clock_sampler(dev):
+    """NVML sampler where the driver's library answers, else nvidia-smi."""
+    try:
+        return NvmlSampler(dev)
+    except Exception:
+        return ClockSampler(dev.index)
 
 
 def traffic_from_profile(kernel_src_hash: str, workload: str, units_scale: float):
@@ -300,7 +383,7 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clocks:
+    with clock_sampler(dev) as clocks:
         wall0 = time.perf_counter()
         for i in range(K):
             starts[i].record(stream)
