@@ -318,7 +318,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -490,7 +490,8 @@ def main():
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_per_step_median": float(np.median(step_ms)), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxf8f6f4 (e4m3 x e2m1, ue8m0/32, fp32 accum, bf16 out)",
         "data": "synthetic (seeded numpy generator; random-init expert weights)",
         "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k, "tile_n": tile_n,
