@@ -53,3 +53,17 @@ def test_skewed_routing_structure():
     assert (counts == 0).sum() >= 20
     assert counts.max() >= 3000
     assert w.T % 128 != 0
+
+
+def test_skewed_outlier_rows():
+    # 1 % of the 4000 rows (40, distinct) scaled by 64 = 2^6 before encoding: their
+    # block exponents sit about 6 above the rest
+    w = synth.WORKLOADS["skewed"]
+    codes, sf = synth._activations(w)
+    sfb = sf.view(np.uint8).reshape(w.T, -1).astype(np.int32)
+    row_mean = sfb.mean(axis=1)
+    typical = np.median(row_mean)
+    hot = np.flatnonzero(row_mean > typical + 3)
+    assert len(hot) == 40
+    assert np.all(np.abs(row_mean[hot] - typical - 6) < 1)
+    assert codes.shape == (w.T, w.H) and codes.dtype == np.uint8
