@@ -4,9 +4,11 @@
  * smoke check and by the benchmark's CPU-baseline leg, never by the product
  * path.  It shares no code with the CUDA kernels.
  *
- * Sources it follows (page titles as printed on the pages):
+ * Sources it follows (titles and section names in English translation; the
+ * printed titles follow in brackets):
  *  - "MegaMoE: fusing the MoE forward into one comm/compute kernel"
- *    (code-reading notes), section "Stage 3: FP8 x FP4 two-layer GEMM"
+ *    [MegaMoE：把 MoE 前向路径压进一个通信计算融合核] (code-reading notes),
+ *    section "Stage 3: FP8 x FP4 two-layer GEMM"
  *    (layer equations Z_e = X_e W1_e^T, Y_e = H_e W2_e^T), "Stage 4: SwiGLU
  *    and requantisation in the L1 epilogue" (gate/up cast to BF16 first,
  *    silu(a) = a / (1 + exp(-a)), times the top-k weight, per-32-channel
@@ -15,9 +17,10 @@
  *    equation y_t = sum_j g_tj W2 SwiGLU(W1 x_t) of "Problem background".
  *  - "MegaMoE" blog, section 7.3 "L1 weight interleave" (gate/up rows
  *    interleaved with granularity 8) and 7.1 "precision configuration".
- *  - "Fused comm/compute operators (5): practice", section 2 "schedule
- *    tables" (expert-sorted pool, each expert padded to 128 rows, one slot
- *    table [token][k], slack per 128-row block).
+ *  - "Fused comm/compute operators (5): practice" [通算融合算子（五）：实战——
+ *    两个 kernel 写完一个 TP MoE 融合层], section 2 "schedule tables"
+ *    (expert-sorted pool, each expert padded to 128 rows, one slot table
+ *    [token][k], slack per 128-row block).
  *
  * Readings taken where the pages are silent or garbled (all listed in the
  * design notes): OCP MX element formats (E4M3 bias 7 max 448 no Inf;
