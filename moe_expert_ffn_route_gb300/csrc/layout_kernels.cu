@@ -1,7 +1,9 @@
 // Routing, schedule-table, gather, combine and weight-preparation kernels
 // of the fused MoE expert forward (everything except the two grouped GEMMs).
 //
-// Sources (page titles as printed, sections):
+// Sources (page titles and sections, in English translation where the page
+// is Chinese: the practice page is 通算融合算子（五）：实战, the notes are
+// MegaMoE：把 MoE 前向路径压进一个通信计算融合核):
 //  - MegaMoE blog 4.2 "Dispatch warps": per-expert counting with block-local
 //    atomics over all (token, k) entries, then the pull of each routed
 //    token's hidden vector into the expert pool (here a local gather).
