@@ -47,30 +47,6 @@
 
 namespace moeffn {
 
-// Optional timeline of CTA 0 of layer L (build with -DMOEFFN_TRACE=L): SM
-// clock stamps around every wait and issue of the load, MMA and epilogue roles.
-#ifdef MOEFFN_TRACE
-constexpr int kTraceEvents = 4096;
-// roles 0-2: load, MMA, epilogue of CTA 0; roles 3-4: load, forwarder of CTA 1
-__device__ unsigned long long g_trace[5][kTraceEvents][3];
-__device__ int g_trace_n[5];
-static int g_trace_grid = 0;
-#define TRACE_STAMP(v) (v) = clock64()
-#define TRACE_PUT(role, i, a, b, c)                                                           \
-    do {                                                                                      \
-        const int r_ = (role) + (blockIdx.x == 1 ? 3 : 0);                                    \
-        if (blockIdx.x < 2 && r_ < 5 && LAYER == MOEFFN_TRACE && (i) < kTraceEvents) {         \
-            g_trace[r_][i][0] = (a);                                                          \
-            g_trace[r_][i][1] = (b);                                                          \
-            g_trace[r_][i][2] = (c);                                                          \
-            g_trace_n[r_] = (i) + 1;                                                          \
-        }                                                                                     \
-    } while (0)
-#else
-#define TRACE_STAMP(v) (void)0
-#define TRACE_PUT(role, i, a, b, c) (void)0
-#endif
-
 // warp roles: 0..11 drain TMEM (three warps per lane quarter, taking every
 // third 32-column chunk); 12 and 13 issue the MMAs of the even and the odd
 // tiles of the pair (leader) or forward "stage loaded" of those tiles (peer);
@@ -261,8 +237,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int pw = (warp - kFirstProducerWarp) % C::PRODUCERS;
         {
             // the whole warp runs the loop; one elected lane issues each copy
-            int ls = 0, ntr = 0;                         // stage within the ring
-            (void)ntr;
+            int ls = 0;                                  // stage within the ring
             uint32_t phase = 0;
             uint32_t armed[C::RING] = {};
             const bool starve = LAYER == 1 && (p.debug_flags & 1) && rank == 0 && ring == 0;
@@ -292,14 +267,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         continue;
                     }
                     const int stage = ring * C::RING + ls;
-                    unsigned long long c0 = 0, c1 = 0, c2 = 0;
-                    TRACE_STAMP(c0);
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded(empty(stage), phase ^ 1u, abort_flag,
                                                                     p.timeout_ns, p.status, 1))) {
                         ok = false;
                         break;
                     }
-                    TRACE_STAMP(c1);
                     const uint32_t sb = sbase + stage * C::STAGE_BYTES;
                     const uint32_t ss = sfbase + stage * C::SF_STAGE;
                     if (!(starve && t == pair && kb == 0)) {
@@ -310,9 +282,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         bulk_load_w(ss + 512, sfb + kb * 1024, C::SFB_BYTES, full(stage));
                         ++armed[ls];
                     }
-                    TRACE_STAMP(c2);
-                    if (lane == 0 && pw == 0 && ring == 0) TRACE_PUT(0, ntr, c0, c1, c2);
-                    ++ntr;
                     if (++ls == C::RING) {
                         ls = 0;
                         phase ^= 1u;
@@ -334,23 +303,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             // in ring order: once this CTA's copies of a stage have landed,
             // arrive on the leader's barrier of that stage
             const uint32_t remote_full0 = map_shared_rank(full(0), 0);
-            int ls = 0, ntr = 0;
-            (void)ntr;
+            int ls = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (int t = pair + ring * npairs; t < total && ok; t += 2 * npairs) {
                 for (int kb = 0; kb < nkb; ++kb) {
                     const int stage = ring * C::RING + ls;
-                    unsigned long long c0 = 0, c1 = 0;
-                    TRACE_STAMP(c0);
                     if (!mbar_wait_bounded(full(stage), phase, abort_flag, p.timeout_ns, p.status, 7)) {
                         ok = false;
                         break;
                     }
-                    TRACE_STAMP(c1);
                     mbar_arrive_remote_relaxed(remote_full0 + 8u * stage);
-                    if (ring == 0) TRACE_PUT(1, ntr, c0, c1, c1);
-                    ++ntr;
                     if (++ls == C::RING) {
                         ls = 0;
                         phase ^= 1u;
@@ -361,8 +324,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             // ---------------------------------------------------- MMA (leader)
             // the whole warp runs the loop; one elected lane issues each instruction
             constexpr uint32_t IDESC = idesc_mx_e2m1_e4m3(256, 0);
-            int ls = 0, it = 0, ntr = 0;
-            (void)ntr;
+            int ls = 0, it = 0;
             uint32_t phase = 0, kiter = 0;
             bool ok = true;
             const uint32_t sf_base = tmem + C::SF_COL + static_cast<uint32_t>(ring * 2 * C::SF_SET_COLS);
@@ -387,14 +349,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     idk[k] = idesc_n | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
                 for (int kb = 0; kb < nkb; ++kb) {
                     const int stage = ring * C::RING + ls;
-                    unsigned long long c0 = 0, c1 = 0, c2 = 0;
-                    TRACE_STAMP(c0);
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded(full(stage), phase, abort_flag, p.timeout_ns,
                                                                     p.status, 3))) {
                         ok = false;
                         break;
                     }
-                    TRACE_STAMP(c1);
                     tc_fence_after();
                     const uint32_t sb = sbase + stage * C::STAGE_BYTES;
                     const uint32_t ss = sfbase + stage * C::SF_STAGE;
@@ -410,9 +369,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tc_mma_mx_pair_w(d, adesc + 4, bdesc + 4, idk[2], sfs, sfs + 4, 1u);
                     tc_mma_mx_pair_w(d, adesc + 6, bdesc + 6, idk[3], sfs, sfs + 4, 1u);
                     tc_commit_pair_w(empty(stage));
-                    TRACE_STAMP(c2);
-                    if (lane == 0 && ring == 0) TRACE_PUT(1, ntr, c0, c1, c2);
-                    ++ntr;
                     if (++ls == C::RING) {
                         ls = 0;
                         phase ^= 1u;
@@ -439,8 +395,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (t + npairs < total) rec = load_rec(t + npairs, ncb, p);
             const int as = it % ACC;
             const uint32_t ap = static_cast<uint32_t>(it / ACC) & 1u;
-            unsigned long long e0 = 0, e1 = 0, e2 = 0;
-            TRACE_STAMP(e0);
             const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(tfull(as), ap, abort_flag, p.timeout_ns,
                                                                         p.status, 4));
             if constexpr (LAYER == 1) {
@@ -455,7 +409,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             } else if (!got) {
                 break;
             }
-            TRACE_STAMP(e1);
             tc_fence_after();
             const uint32_t tacc = tq + static_cast<uint32_t>(as * RW);
             const int nchunks = (ti.nvalid + 31) / 32;
@@ -616,8 +569,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             // complete (tcgen05.wait::ld) and fenced above; the rows stored to global
             // memory are not read by that warp, and a release would wait for them
             if (lane == 0) mbar_arrive_remote_relaxed(leader_tempty0 + 8u * as);
-            TRACE_STAMP(e2);
-            if (warp == 0 && lane == 0) TRACE_PUT(2, it, e0, e1, e2);
         }
     }
 
@@ -629,14 +580,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         tmem_dealloc_pair(tmem, C::TMEM_COLS);
     }
 }
-
-#ifdef MOEFFN_TRACE
-extern "C" __attribute__((visibility("default"))) int moeffn_trace_read(unsigned long long* out, int* counts) {
-    if (cudaMemcpyFromSymbol(out, g_trace, sizeof(g_trace)) != cudaSuccess) return -1;
-    if (cudaMemcpyFromSymbol(counts, g_trace_n, sizeof(g_trace_n)) != cudaSuccess) return -1;
-    return g_trace_grid;
-}
-#endif
 
 template <int LAYER, int BN, int RW>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap* tmB, const GemmArgs& a,
@@ -662,9 +605,6 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap* tmB, co
         clusters = a.num_sms / 2;
     }
     cfg.gridDim = dim3(2 * (clusters < a.num_sms / 2 ? clusters : a.num_sms / 2), 1, 1);
-#ifdef MOEFFN_TRACE
-    if (LAYER == MOEFFN_TRACE) g_trace_grid = static_cast<int>(cfg.gridDim.x);
-#endif
     TokenMaps maps;
     for (int i = 0; i < kNumTokenBoxes; ++i) maps.m[i] = tmB[i];
     err = cudaLaunchKernelEx(&cfg, kernel, tmA, maps, a);
