@@ -39,7 +39,10 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
         const int e = lane + 32 * i;
-        v[i] = e < E ? __ldg(l + e) : -INFINITY;
+        // a NaN logit ranks below every number, like -inf: every candidate
+        // then compares, and each round picks a valid, untaken expert
+        const float x = e < E ? __ldg(l + e) : -INFINITY;
+        v[i] = x == x ? x : -INFINITY;
         if (e >= E) taken |= 1u << i;
     }
     float my_v = 0.f;
@@ -64,7 +67,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                 be = oe;
             }
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (be < E && (be & 31) == lane) taken |= 1u << (be >> 5);
         if (lane == j) {
             my_v = bv;
             my_e = be;

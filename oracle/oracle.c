@@ -129,15 +129,19 @@ int oracle_requant_exponent(double amax) {
 /* routing: softmax over router logits, top-k, renormalise                  */
 /* ------------------------------------------------------------------------ */
 
+/* The pages do not say what a NaN router logit means; it is read here as
+ * -inf: it ranks below every number and has softmax weight 0. */
 void oracle_route(const float* logits, int T, int E, int k, int64_t* idx, float* w) {
     double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    double* l = (double*)malloc(sizeof(double) * (size_t)E);
     char* taken = (char*)malloc((size_t)E);
     for (int t = 0; t < T; ++t) {
-        const float* l = logits + (size_t)t * E;
+        const float* lt = logits + (size_t)t * E;
+        for (int e = 0; e < E; ++e) l[e] = isnan(lt[e]) ? -INFINITY : (double)lt[e];
         double lmax = -INFINITY;
         for (int e = 0; e < E; ++e) if (l[e] > lmax) lmax = l[e];
         double z = 0.0;
-        for (int e = 0; e < E; ++e) { p[e] = exp((double)l[e] - lmax); z += p[e]; }
+        for (int e = 0; e < E; ++e) { p[e] = exp(l[e] - lmax); z += p[e]; }
         for (int e = 0; e < E; ++e) p[e] /= z;             /* softmax */
         memset(taken, 0, (size_t)E);
         double sel = 0.0;
@@ -155,6 +159,7 @@ void oracle_route(const float* logits, int T, int E, int k, int64_t* idx, float*
             w[(size_t)t * k + j] = (float)(p[idx[(size_t)t * k + j]] / sel);
     }
     free(p);
+    free(l);
     free(taken);
 }
 

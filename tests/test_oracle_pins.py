@@ -144,6 +144,31 @@ def test_route_bruteforce_small():
             assert abs(w[t].astype(np.float64).sum() - 1) < 1e-6
 
 
+def test_route_nan_logits_rank_last():
+    """The pages leave NaN router logits undefined; the reading taken is that a
+    NaN ranks below every number.  Checked against torch's top-k over the
+    logits with NaN replaced by -inf (torch.sort is stable: ties keep the
+    lower index first) and torch's softmax over the chosen values."""
+    rng = np.random.default_rng(12)
+    T, E, k = 64, 40, 6
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[rng.random((T, E)) < 0.3] = np.nan
+    logits[5, :E - 3] = np.nan                  # fewer finite logits than k
+    logits[5, E - 3:] = [0.5, -1.0, 2.0]
+    logits[6, 0] = -np.inf
+    idx, w = oracle.route(logits, k)
+    clean = torch.from_numpy(np.where(np.isnan(logits), -np.inf, logits).astype(np.float64))
+    order = torch.sort(clean, dim=1, descending=True, stable=True).indices[:, :k]
+    assert np.array_equal(idx, order.numpy())
+    sel = torch.gather(clean, 1, order)
+    ref = torch.softmax(sel, 1).numpy()
+    ok = np.isfinite(sel.numpy()).all(axis=1)
+    assert np.allclose(w[ok], ref[ok], rtol=2e-7, atol=1e-30)
+    # with fewer than k finite logits the -inf entries get weight 0
+    assert np.all(w[5, 3:] == 0) and np.allclose(w[5, :3].sum(), 1.0, rtol=1e-6)
+    assert sorted(idx[5, 3:].tolist()) == list(range(3))
+
+
 # ---------------------------------------------------------------- layout
 
 def _check_layout(idx, E, lay, block=128):
