@@ -230,8 +230,8 @@ MOEFFN_API moeffn_status moeffn_query(const moeffn_problem* problem, void* works
  * Word [1] names the first wait that ran out: 1 a TMA producer (stage free),
  * 2 an MMA warp (accumulator drained), 3 an MMA warp (stage loaded),
  * 4 the epilogue (accumulator ready), 5 and 6 the end-of-kernel drains of
- * copies and MMAs, 7 the second CTA of a pair (stage loaded).  With a whole
- * grid waiting on one failure, which of them expires first is a race. */
+ * copies and MMAs.  With a whole grid waiting on one failure, which of them
+ * expires first is a race. */
 MOEFFN_API moeffn_status moeffn_get_device_status(const moeffn_problem* problem, void* workspace,
                                        moeffn_stream stream, uint32_t* detail);
 
@@ -251,9 +251,12 @@ MOEFFN_API moeffn_status moeffn_get_device_status(const moeffn_problem* problem,
  * Needs 64 + 4*T*k + 4*ceil(T*k/1024)*E bytes of the static scratch; larger
  * problems return MOEFFN_ERR_WORKSPACE_TOO_SMALL before anything runs.
  * Limits on T, E, k as moeffn_route_topk.  Allocates nothing and frees
- * nothing.  The first call on a device looks up the array's device address
- * (with that device current); make that first call before any stream
- * capture.  All calls share the array and it keeps the last call's
+ * nothing once the library is loaded on the device: with lazy module
+ * loading (the CUDA default) the first call on a device loads the
+ * library's device code, which reserves the array and may synchronise, so
+ * make one call on each device at start-up, before any stream capture.
+ * Every call looks up the array's device address with the calling thread's
+ * current device.  All calls share the array and it keeps the last call's
  * contents: calls that overlap on the GPU race and give wrong tables. */
 #define MOEFFN_NOALLOC_SCRATCH_BYTES (4u << 20)
 MOEFFN_API moeffn_status moeffn_schedule_tables_noalloc(const int64_t* topk_idx, int32_t num_tokens,

@@ -163,6 +163,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t k, uint64_t rows, uint3
     return r == CUDA_SUCCESS;
 }
 
+// Scale array read as rows of `row_words` 32-bit words, one row per box.
+bool make_sf_map(CUtensorMap* m, const void* base, uint64_t row_words, uint64_t rows, uint32_t box_words) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {row_words, rows};
+    const cuuint64_t strides[1] = {row_words * 4};
+    const cuuint32_t box[2] = {box_words, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -288,13 +302,20 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
 
     const PrepLayout PL = prep_layout(*p);
     const uint8_t* pb = static_cast<const uint8_t*>(prepared);
-    CUtensorMap a1, a2, b1[kNumTokenBoxes], b2[kNumTokenBoxes];
-    if (!make_map(&a1, pb + PL.w1p, H, static_cast<uint64_t>(E) * 2 * I, 128, true) ||
-        !make_map(&a2, pb + PL.w2p, I, static_cast<uint64_t>(E) * H, 128, true))
+    GemmMaps m1, m2;
+    const uint64_t kb1 = H / 128, kb2 = I / 128;
+    if (!make_map(&m1.a, pb + PL.w1p, H, static_cast<uint64_t>(E) * 2 * I, 128, true) ||
+        !make_map(&m2.a, pb + PL.w2p, I, static_cast<uint64_t>(E) * H, 128, true) ||
+        !make_sf_map(&m1.sfa, pb + PL.w1p_sf, 128, static_cast<uint64_t>(E) * (2 * I / 128) * kb1, 128) ||
+        !make_sf_map(&m2.sfa, pb + PL.w2p_sf, 128, static_cast<uint64_t>(E) * (H / 128) * kb2, 128) ||
+        !make_sf_map(&m1.sfb_512, w + L.xpool_sf, 256, static_cast<uint64_t>(L.NT_max) * kb1, 128) ||
+        !make_sf_map(&m1.sfb_1k, w + L.xpool_sf, 256, static_cast<uint64_t>(L.NT_max) * kb1, 256) ||
+        !make_sf_map(&m2.sfb_512, w + L.hpool_sf, 256, static_cast<uint64_t>(L.NT_max) * kb2, 128) ||
+        !make_sf_map(&m2.sfb_1k, w + L.hpool_sf, 256, static_cast<uint64_t>(L.NT_max) * kb2, 256))
         return MOEFFN_ERR_CUDA;
     for (int i = 0; i < kNumTokenBoxes; ++i)
-        if (!make_map(&b1[i], w + L.xpool, H, L.P_max, 8 * (i + 1), false) ||
-            !make_map(&b2[i], w + L.hpool, I, L.P_max, 8 * (i + 1), false))
+        if (!make_map(&m1.b[i], w + L.xpool, H, L.P_max, 8 * (i + 1), false) ||
+            !make_map(&m2.b[i], w + L.hpool, I, L.P_max, 8 * (i + 1), false))
             return MOEFFN_ERR_CUDA;
 
     GemmArgs g{};
@@ -315,13 +336,9 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
     g.num_sms = num_sms;
     g.tile_n = tile_n;
 
-    g.sfa = pb + PL.w1p_sf;
-    g.sfb = w + L.xpool_sf;
-    if (launch_gemm(1, a1, b1, g, st) != cudaSuccess || !mark(2)) return MOEFFN_ERR_CUDA;
+    if (launch_gemm(1, m1, g, st) != cudaSuccess || !mark(2)) return MOEFFN_ERR_CUDA;
     if (p->debug_flags & MOEFFN_DEBUG_DUMP_L1_ACC) return MOEFFN_OK;   // accumulators left in the output pool
-    g.sfa = pb + PL.w2p_sf;
-    g.sfb = w + L.hpool_sf;
-    if (launch_gemm(2, a2, b2, g, st) != cudaSuccess || !mark(3)) return MOEFFN_ERR_CUDA;
+    if (launch_gemm(2, m2, g, st) != cudaSuccess || !mark(3)) return MOEFFN_ERR_CUDA;
 
     if (launch_combine(reinterpret_cast<const uint16_t*>(w + L.ypool), slots, T, H, k, y, st) != cudaSuccess ||
         !mark(4))

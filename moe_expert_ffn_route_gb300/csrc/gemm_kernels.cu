@@ -49,8 +49,9 @@ namespace moeffn {
 
 // warp roles: 0..11 drain TMEM (three warps per lane quarter, taking every
 // third 32-column chunk); 12 and 13 issue the MMAs of the even and the odd
-// tiles of the pair (leader) or forward "stage loaded" of those tiles (peer);
-// 14 and 15 issue the TMA copies of the two rings of stages.  The MMA and TMA
+// tiles of the pair (leader; idle in the peer); 14 and 15 issue the TMA
+// copies of the two rings of stages (both CTAs; the copies of both signal
+// the leader's barrier of the stage).  The MMA and TMA
 // warps issue from all 32 lanes through elect.sync: issued from one lane of a
 // divergent branch a block-scaled MMA costs about twice its tensor-pipe time.
 constexpr int kEpiWarps = 12;
@@ -128,6 +129,8 @@ __device__ __forceinline__ int box_half_rows(int box) {
     return 8 * (box + 1);
 }
 
+static_assert(sizeof(GemmMaps::b) / sizeof(CUtensorMap) == kNumTokenBoxes, "one token map per box height");
+
 struct TileInfo {
     int e, cb, tile_idx, row0, nvalid, ncols;   // ncols: pair MMA N (the expert's tile rows, a multiple of 16)
 };
@@ -174,6 +177,7 @@ __device__ __forceinline__ void pair_sync(int pi) {
 template <int LAYER, int BN, int RW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, RW>::THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TokenMaps tmB,
+                    const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                     const GemmArgs p) {
     using C = GemmCfg<BN, RW>;
     constexpr int S = C::STAGES, ACC = C::NACC;
@@ -199,8 +203,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t rank = cluster_cta_rank();           // 0: leader (issues the MMAs), 1: peer
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            // the leader's "stage full" also waits for the peer's forwarded arrival
-            mbar_init(full(s), rank == 0 ? 2 : 1);
+            // the leader's "stage full" counts the bytes of both CTAs' copies
+            // (they signal it directly); the peer's own is unused
+            mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
         for (int a = 0; a < ACC; ++a) {
@@ -211,6 +216,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmSFA);
+        prefetch_tensormap(&tmSFB);
         for (int i = 0; i < kNumTokenBoxes; ++i) prefetch_tensormap(&tmB.m[i]);
     }
     if (warp == kFirstMmaWarp) {
@@ -219,7 +226,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();                                      // both CTAs' barriers exist before any remote arrive
+    cluster_sync();                                      // both CTAs' barriers exist before any copy signals one
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_wait();                                          // the previous kernel's tables and pools are written
@@ -236,7 +243,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int ring = (warp - kFirstProducerWarp) / C::PRODUCERS;
         const int pw = (warp - kFirstProducerWarp) % C::PRODUCERS;
         {
-            // the whole warp runs the loop; one elected lane issues each copy
+            // the whole warp runs the loop; one elected lane issues each copy.
+            // Both CTAs' copies of a stage signal the leader's "stage full",
+            // which the leader arms with the bytes of both halves.
+            const uint32_t leader_full0 = map_shared_rank(full(0), 0);
             int ls = 0;                                  // stage within the ring
             uint32_t phase = 0;
             uint32_t armed[C::RING] = {};
@@ -251,8 +261,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const bool mine_valid = mrow < a_rows;                          // false only for an L2 tail half
                 const int a0 = ti.e * a_rows + mrow;
                 const int sf_block = (ti.e * a_rows + (mine_valid ? mrow : ti.cb * 256)) / 128;
-                const uint8_t* sfa = p.sfa + static_cast<size_t>(sf_block) * nkb * 512;
-                const uint8_t* sfb = p.sfb + static_cast<size_t>(ti.tile_idx) * nkb * 1024;
+                const int sfa_row = sf_block * nkb;          // rows of 512 B: one per 128-row block and K block
+                const int sfb_row = ti.tile_idx * nkb;       // rows of 1 KB: one per token tile and K block
                 const int half = ti.ncols / 2;
                 const int box = box_for_half(half);
                 const CUtensorMap* tmBox = &tmB.m[box];
@@ -275,11 +285,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t sb = sbase + stage * C::STAGE_BYTES;
                     const uint32_t ss = sfbase + stage * C::SF_STAGE;
                     if (!(starve && t == pair && kb == 0)) {
-                        mbar_arrive_expect_tx_w(full(stage), bytes);
-                        tma_load_2d_w(sb, &tmA, full(stage), kb * 128, a0);
-                        tma_load_2d_w(sb + C::A_BYTES, tmBox, full(stage), kb * 128, brow);
-                        bulk_load_w(ss, sfa + kb * 512, 512, full(stage));
-                        bulk_load_w(ss + 512, sfb + kb * 1024, C::SFB_BYTES, full(stage));
+                        const uint32_t fb = leader_full0 + 8u * stage;
+                        if (rank == 0) mbar_arrive_expect_tx_w(full(stage), 2 * bytes);
+                        tma_load_2d_pair_w(sb, &tmA, fb, kb * 128, a0);
+                        tma_load_2d_pair_w(sb + C::A_BYTES, tmBox, fb, kb * 128, brow);
+                        tma_load_2d_pair_w(ss, &tmSFA, fb, 0, sfa_row + kb);
+                        tma_load_2d_pair_w(ss + 512, &tmSFB, fb, 0, sfb_row + kb);
                         ++armed[ls];
                     }
                     if (++ls == C::RING) {
@@ -288,39 +299,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 }
             }
-            // never leave copies in flight into shared memory: wait for the last
-            // arming of every owned stage to land (immediate on the normal path)
-            for (int l = 0; l < C::RING; ++l)
-                if (armed[l])
-                    mbar_wait_bounded(full(ring * C::RING + l), (armed[l] - 1u) & 1u, abort_flag, p.timeout_ns,
-                                      p.status, 5, false);
+            // never leave copies in flight into shared memory: the leader waits
+            // for the last arming of every stage of its ring to land (immediate
+            // on the normal path; it counts the peer's bytes too).  The peer's
+            // copies are consumed by the leader's MMAs before the pair's final
+            // cluster barrier; after a timeout the peer leaves its loop only once
+            // its own bounded wait for a free stage ran out, long after its last
+            // copies landed.
+            if (rank == 0)
+                for (int l = 0; l < C::RING; ++l)
+                    if (armed[l])
+                        mbar_wait_bounded(full(ring * C::RING + l), (armed[l] - 1u) & 1u, abort_flag,
+                                          p.timeout_ns, p.status, 5, false);
         }
         __syncwarp();
     } else if (warp >= kFirstMmaWarp) {
         const int ring = warp - kFirstMmaWarp;               // tiles of this parity, accumulator `ring`
-        if (lane == 0 && rank == 1) {
-            // ---------------------------------------------------- forwarder (peer)
-            // in ring order: once this CTA's copies of a stage have landed,
-            // arrive on the leader's barrier of that stage
-            const uint32_t remote_full0 = map_shared_rank(full(0), 0);
-            int ls = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int t = pair + ring * npairs; t < total && ok; t += 2 * npairs) {
-                for (int kb = 0; kb < nkb; ++kb) {
-                    const int stage = ring * C::RING + ls;
-                    if (!mbar_wait_bounded(full(stage), phase, abort_flag, p.timeout_ns, p.status, 7)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_remote_relaxed(remote_full0 + 8u * stage);
-                    if (++ls == C::RING) {
-                        ls = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-        } else if (rank == 0) {
+        if (rank == 0) {
             // ---------------------------------------------------- MMA (leader)
             // the whole warp runs the loop; one elected lane issues each instruction
             constexpr uint32_t IDESC = idesc_mx_e2m1_e4m3(256, 0);
@@ -582,8 +577,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 }
 
 template <int LAYER, int BN, int RW>
-static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap* tmB, const GemmArgs& a,
-                              cudaStream_t stream) {
+static cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, cudaStream_t stream) {
     using C = GemmCfg<BN, RW>;
     auto kernel = grouped_gemm_kernel<LAYER, BN, RW>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -606,23 +600,22 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap* tmB, co
     }
     cfg.gridDim = dim3(2 * (clusters < a.num_sms / 2 ? clusters : a.num_sms / 2), 1, 1);
     TokenMaps maps;
-    for (int i = 0; i < kNumTokenBoxes; ++i) maps.m[i] = tmB[i];
-    err = cudaLaunchKernelEx(&cfg, kernel, tmA, maps, a);
+    for (int i = 0; i < kNumTokenBoxes; ++i) maps.m[i] = m.b[i];
+    err = cudaLaunchKernelEx(&cfg, kernel, m.a, maps, m.sfa, BN <= 128 ? m.sfb_512 : m.sfb_1k, a);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(int layer, const CUtensorMap& tmA, const CUtensorMap* tmB, const GemmArgs& a,
-                        cudaStream_t stream) {
+cudaError_t launch_gemm(int layer, const GemmMaps& m, const GemmArgs& a, cudaStream_t stream) {
     // three stage layouts: tiles of at most 32 rows (10 stages in flight, four
     // accumulator regions), at most 144 rows (8 stages, three regions) and at
     // most kMaxTileN rows (6 stages, two regions)
     if (a.tile_n <= 32)
-        return layer == 1 ? launch_one<1, 32, 32>(tmA, tmB, a, stream) : launch_one<2, 32, 32>(tmA, tmB, a, stream);
+        return layer == 1 ? launch_one<1, 32, 32>(m, a, stream) : launch_one<2, 32, 32>(m, a, stream);
     if (a.tile_n <= 144)
-        return layer == 1 ? launch_one<1, 144, 144>(tmA, tmB, a, stream) : launch_one<2, 144, 144>(tmA, tmB, a, stream);
-    return layer == 1 ? launch_one<1, kMaxTileN, kMaxTileN>(tmA, tmB, a, stream)
-                      : launch_one<2, kMaxTileN, kMaxTileN>(tmA, tmB, a, stream);
+        return layer == 1 ? launch_one<1, 144, 144>(m, a, stream) : launch_one<2, 144, 144>(m, a, stream);
+    return layer == 1 ? launch_one<1, kMaxTileN, kMaxTileN>(m, a, stream)
+                      : launch_one<2, kMaxTileN, kMaxTileN>(m, a, stream);
 }
 
 }  // namespace moeffn

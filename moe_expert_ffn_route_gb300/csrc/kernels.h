@@ -51,8 +51,6 @@ struct GemmArgs {
     const int* tile_rec;     // per token tile: its expert's tile record (LayoutArgs)
     int E;
     int H, I;
-    const uint8_t* sfa;     // prepared weight scales (per 128-row block, per K block)
-    const uint8_t* sfb;     // pool scales (per token tile, per K block)
     const float* wpool;
     uint8_t* hpool;         // L1 output [P_max][I]
     uint8_t* hpool_sf;      // L1 output scales (per token tile, per K block of L2)
@@ -72,9 +70,18 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const uint16_t* ypool, const int* slots, int T, int H, int k,
                            uint16_t* y, cudaStream_t stream);
 cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t stream);
-// layer = 1 or 2; tmap_a over the prepared weights, tmap_b[4] over the pool
-// with boxes of 16, 32, 64 and kMaxTileN/2 token rows (half a pair's tile)
-cudaError_t launch_gemm(int layer, const CUtensorMap& tmap_a, const CUtensorMap* tmap_b,
-                        const GemmArgs& a, cudaStream_t stream);
+// Tensor maps of one grouped GEMM launch: the prepared weights (boxes of
+// 128 rows x 128 K), the token pool (boxes of 8, 16, ..., kMaxTileN/2 rows,
+// half a pair's tile), and the scale arrays as rows of 512 B (weights: one
+// per 128-row block and K block) and of 1 KB (pool: one per token tile and K
+// block), read as boxes of one row (512 B or 1 KB of the pool row).
+struct GemmMaps {
+    CUtensorMap a;
+    CUtensorMap b[14];
+    CUtensorMap sfa;
+    CUtensorMap sfb_512, sfb_1k;
+};
+// layer = 1 or 2
+cudaError_t launch_gemm(int layer, const GemmMaps& maps, const GemmArgs& a, cudaStream_t stream);
 
 }  // namespace moeffn
