@@ -16,8 +16,6 @@
 #include "moeffn.h"
 #include "common.cuh"
 
-#include <mutex>
-
 namespace {
 
 using moeffn::DevStatus;
@@ -131,21 +129,17 @@ __global__ void __launch_bounds__(kChunk) sched_tables_noalloc_kernel(
     if (tid == 0) st->done_counter = 0;
 }
 
-// Device address of g_sched_scratch, looked up once per device with that
-// device current (the host-side name of the array is not a device address).
-std::mutex g_mu;
-void* g_scratch_ptr[64] = {nullptr};
-
+// Device address of g_sched_scratch on the current device (the host-side
+// name of the array is not a device address).  Looked up on every call: once
+// the library's module is loaded on the device this is a host-side table
+// lookup, and it stays right if the context was torn down and the module
+// reloaded at another address.  With lazy module loading (the default since
+// CUDA 12.2) the first lookup on a device loads the module, which reserves
+// the array; that is why callers make their first call at start-up.
 moeffn_status scratch_for_current_device(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOEFFN_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_sched_scratch) != cudaSuccess || !p) return MOEFFN_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sched_scratch) != cudaSuccess || !p) return MOEFFN_ERR_CUDA;
+    *out = p;
     return MOEFFN_OK;
 }
 
