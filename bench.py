@@ -6,6 +6,11 @@ logits, then the fused expert forward (schedule tables + gather, L1 grouped
 GEMM + SwiGLU/requant epilogue, L2 grouped GEMM, combine), all in this
 repository's CUDA kernels through the C ABI.
 
+The headline workload is the prefill shape (T=8192, H=7168, I=2048, E=256,
+top-8), the largest configuration and the compute-bound one; the
+decode shape (T=128, same model) is timed after it in the same run and
+reported under "per_workload" (device-timed, with its own roofline).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 Prints one JSON line.  N > 1 runs under torchrun as independent replicas
@@ -32,7 +37,8 @@ sys.path.insert(0, ROOT)
 from moe_expert_ffn_route_gb300 import synth  # noqa: E402
 
 METRIC = "fused MoE fwd tokens/s & TFLOP/s, % of roofline (1×GB300)"
-DEFAULT_WORKLOAD = "medium"
+DEFAULT_WORKLOAD = "prefill"          # the largest single-GPU configuration (compute-bound)
+ALSO_TIMED = ("decode",)              # timed after the headline in the same run (weight-streaming)
 L2_BYTES = 129 * 1024 * 1024
 KERNELS_PER_STEP = 6      # route, layout count, dispatch/gather, L1 GEMM, L2 GEMM, combine
 
@@ -314,6 +320,118 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+class DeviceRun:
+    """One workload resident on the device: inputs, prepared weights, workspace
+    and output, plus the timed device steps."""
+
+    def __init__(self, wl, dev, mb):
+        import torch
+        self.wl, self.dev, self.mb = wl, dev, mb
+        self.inp = synth.make_inputs(wl)
+        T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+        self.prob = mb.problem(T, H, I, E, k)
+        self.tile_n = mb.tile_n(self.prob)
+
+        def up(a):
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint32:
+                a = a.view(np.int32)
+            return torch.from_numpy(a).to(dev)
+
+        inp = self.inp
+        self.prepared = mb.prepare_weights(self.prob, up(inp["w1"]), up(inp["w1_sf"]), up(inp["w2"]),
+                                           up(inp["w2_sf"]))
+        self.logits, self.x, self.x_sf = up(inp["logits"]), up(inp["x"]), up(inp["x_sf"])
+        self.idx = torch.empty((T, k), dtype=torch.int64, device=dev)
+        self.wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.ws = mb.empty_workspace(self.prob, dev)
+        self.y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream()
+
+    def step(self, events=None, logits=None, x=None, x_sf=None, y=None):
+        """One pass of the whole hot path: routing, then the fused forward."""
+        mb, k = self.mb, self.wl.k
+        logits = self.logits if logits is None else logits
+        x = self.x if x is None else x
+        x_sf = self.x_sf if x_sf is None else x_sf
+        y = self.y if y is None else y
+        mb.route_topk(logits, k, self.idx, self.wts)
+        if events is None:
+            mb.forward(self.prob, x, x_sf, self.idx, self.wts, self.prepared, self.ws, y)
+        else:
+            mb.forward_profiled(self.prob, x, x_sf, self.idx, self.wts, self.prepared, self.ws, y, events)
+
+    def warm(self, W):
+        import torch
+        for _ in range(W):
+            self.step()
+            self.flush.fill_(1)
+        torch.cuda.synchronize()
+        st, code, _ = self.mb.device_status(self.prob, self.ws)
+        if st != self.mb.OK:
+            raise SystemExit(f"device status {self.mb.STATUS[st]} ({code})")
+        counts = self.mb.query(self.prob, self.ws, "counts").view(torch.int32)[: self.wl.E].cpu().numpy()
+        self.alg = algorithmic(self.wl, counts)
+
+    def timed(self, K, world):
+        """K steps, each bracketed by CUDA events on the launching stream, the L2
+        flushed between steps outside the timed intervals; then steps with
+        events between the stages.  Returns (per-step ms, stage ms, clocks, wall s)."""
+        import torch
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with clock_sampler(self.dev) as clocks:
+            wall0 = time.perf_counter()
+            for i in range(K):
+                starts[i].record(self.stream)
+                self.step()
+                ends[i].record(self.stream)
+                self.flush.fill_(i & 0xFF)
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - wall0
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        # per-stage times from separate steps with events between the stages (the
+        # events keep one kernel from starting before the previous one ends, so
+        # these steps are not the timed ones)
+        KP = min(K, 20)
+        stages = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(KP)]
+        for i in range(KP):
+            self.step(stages[i])
+            self.flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        stage_ms = np.array([[ev[j].elapsed_time(ev[j + 1]) for j in range(4)] for ev in stages])
+        return step_ms, stage_ms, clocks.summary(), wall
+
+
+def l1_roofline(alg, l1_ms, pk):
+    """The L1 GEMM launch against the bound its arithmetic intensity sets."""
+    compute_bound = alg["l1_flops"] / (pk["fp8_tflops"] * 1e12) >= alg["l1_bytes"] / (pk["hbm_gbs"] * 1e9)
+    if compute_bound:
+        achieved = alg["l1_flops"] / (l1_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["fp8_tflops"], "unit": "TFLOP/s"}
+    else:
+        achieved = alg["l1_bytes"] / (l1_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = "grouped_gemm_kernel<1> (L1 GEMM + SwiGLU/requant epilogue)"
+    roof["peak_source"] = (f"{pk['source']}: MEASURED_PEAKS bf16 burst x2 (FP8-rate block-scaled MMA)"
+                           if compute_bound else f"{pk['source']}: MEASURED_PEAKS hbm_gbs")
+    return roof
+
+
+def step_roofline_time(alg, pk):
+    return max(alg["flops"] / (pk["fp8_tflops"] * 1e12), alg["bytes"] / (pk["hbm_gbs"] * 1e9))
+
+
+def stage_summary(stage_ms):
+    return {"tables+gather": float(stage_ms[:, 0].mean()), "l1_gemm": float(stage_ms[:, 1].mean()),
+            "l2_gemm": float(stage_ms[:, 2].mean()), "combine": float(stage_ms[:, 3].mean())}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -322,6 +440,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--also", default=",".join(ALSO_TIMED),
+                    help="comma-separated workloads timed after the headline (device-timed only); '' for none")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = synth.WORKLOADS[args.workload]
@@ -340,69 +460,12 @@ def main():
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
 
-    inp = synth.make_inputs(wl)
-    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
-    prob = mb.problem(T, H, I, E, k)
-    tile_n = mb.tile_n(prob)
-
-    def up(a):
-        a = np.ascontiguousarray(a)
-        if a.dtype == np.uint32:
-            a = a.view(np.int32)
-        return torch.from_numpy(a).to(dev)
-
-    prepared = mb.prepare_weights(prob, up(inp["w1"]), up(inp["w1_sf"]), up(inp["w2"]), up(inp["w2_sf"]))
-    logits, x, x_sf = up(inp["logits"]), up(inp["x"]), up(inp["x_sf"])
-    idx = torch.empty((T, k), dtype=torch.int64, device=dev)
-    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
-    ws = mb.empty_workspace(prob, dev)
-    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(events=None):
-        mb.route_topk(logits, k, idx, wts)
-        if events is None:
-            mb.forward(prob, x, x_sf, idx, wts, prepared, ws, y)
-        else:
-            mb.forward_profiled(prob, x, x_sf, idx, wts, prepared, ws, y, events)
-
-    for _ in range(args.warmup):
-        step()
-        flush.fill_(1)
-    torch.cuda.synchronize()
-    st, code, _ = mb.device_status(prob, ws)
-    if st != mb.OK:
-        raise SystemExit(f"device status {mb.STATUS[st]} ({code})")
-    counts = mb.query(prob, ws, "counts").view(torch.int32)[:E].cpu().numpy()
-    alg = algorithmic(wl, counts)
-
+    R = DeviceRun(wl, dev, mb)
+    T, H, k = wl.T, wl.H, wl.k
+    R.warm(args.warmup)
+    alg = R.alg
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with clock_sampler(dev) as clocks:
-        wall0 = time.perf_counter()
-        for i in range(K):
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-            flush.fill_(i & 0xFF)         # L2 flush between steps, outside the timed intervals
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    # per-stage times from separate steps with events between the stages (the
-    # events keep one kernel from starting before the previous one ends, so
-    # these steps are not the timed ones)
-    KP = min(K, 20)
-    stages = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(KP)]
-    for i in range(KP):
-        step(stages[i])
-        flush.fill_(i & 0xFF)
-    torch.cuda.synchronize()
-    stage_ms = np.array([[ev[j].elapsed_time(ev[j + 1]) for j in range(4)] for ev in stages])
+    step_ms, stage_ms, clock_summary, wall = R.timed(K, world)
     total_ms = max_over_ranks(float(sum(step_ms)), dev)
     if world > 1:
         torch.distributed.barrier()
@@ -410,21 +473,23 @@ def main():
     value = whole_job_rate(T * K, world, total_ms)
 
     # e2e through host buffers: pinned inputs -> device, route + forward, y -> pinned host
+    inp = R.inp
     h_logits = torch.from_numpy(inp["logits"]).pin_memory()
     h_x = torch.from_numpy(inp["x"]).pin_memory()
     h_xsf = torch.from_numpy(inp["x_sf"].view(np.int32)).pin_memory()
     h_y = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     h2d = h_logits.numel() * 4 + h_x.numel() + h_xsf.numel() * 4
     d2h = T * H * 2
+    stream = R.stream
     e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
     for i in range(K):
         e_s.record(stream)
-        logits.copy_(h_logits, non_blocking=True)
-        x.copy_(h_x, non_blocking=True)
-        x_sf.copy_(h_xsf, non_blocking=True)
-        step()
-        h_y.copy_(y, non_blocking=True)
+        R.logits.copy_(h_logits, non_blocking=True)
+        R.x.copy_(h_x, non_blocking=True)
+        R.x_sf.copy_(h_xsf, non_blocking=True)
+        R.step()
+        h_y.copy_(R.y, non_blocking=True)
         e_e.record(stream)
         torch.cuda.synchronize()
         e2e_ms += e_s.elapsed_time(e_e)
@@ -435,8 +500,8 @@ def main():
     # step i overlap the kernels of steps i - 1 and i + 1 (every step still moves
     # its own inputs in and its own y out inside the timed region)
     cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    sets = [{"logits": torch.empty_like(logits), "x": torch.empty_like(x), "x_sf": torch.empty_like(x_sf),
-             "y": torch.empty_like(y)} for _ in range(2)]
+    sets = [{"logits": torch.empty_like(R.logits), "x": torch.empty_like(R.x), "x_sf": torch.empty_like(R.x_sf),
+             "y": torch.empty_like(R.y)} for _ in range(2)]
     h_ys = [h_y, torch.empty((T, H), dtype=torch.bfloat16).pin_memory()]
     ready, done, out_done = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
     p_s, p_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -455,8 +520,7 @@ def main():
         stream.wait_event(ready[b])
         if i >= 2:
             stream.wait_event(out_done[b])     # step i - 2's y has left this set
-        mb.route_topk(S["logits"], k, idx, wts)
-        mb.forward(prob, S["x"], S["x_sf"], idx, wts, prepared, ws, S["y"])
+        R.step(logits=S["logits"], x=S["x"], x_sf=S["x_sf"], y=S["y"])
         done[b].record(stream)
         cout.wait_event(done[b])
         with torch.cuda.stream(cout):
@@ -466,27 +530,41 @@ def main():
     torch.cuda.synchronize()
     e2e_pipe_ms = max_over_ranks(p_s.elapsed_time(p_e), dev)
 
+    # further workloads, device-timed in the same process (the other configuration
+    # the throughput target names: decode, weight-streaming)
+    pk = peaks()
+    also = {}
+    for name in [a for a in args.also.split(",") if a and a != wl.name]:
+        R2 = DeviceRun(synth.WORKLOADS[name], dev, mb)
+        R2.warm(args.warmup)
+        s2, st2, c2, _ = R2.timed(K, world)
+        ms2 = max_over_ranks(float(sum(s2)), dev) / K
+        w2 = R2.wl
+        also[name] = {
+            "config": {"workload": name, "T": w2.T, "H": w2.H, "I": w2.I, "E": w2.E, "k": w2.k,
+                       "tile_n": R2.tile_n, "touched_experts": R2.alg["touched"]},
+            "value": whole_job_rate(w2.T * K, world, ms2 * K), "unit": "tokens/s",
+            "ms_per_step": ms2, "ms_per_step_median": float(np.median(s2)),
+            "tflops": R2.alg["flops"] / (ms2 / 1e3) / 1e12 * world,
+            "hbm_gbs": R2.alg["bytes"] / (ms2 / 1e3) / 1e9,
+            "roofline_step_frac": step_roofline_time(R2.alg, pk) / (ms2 / 1e3),
+            "stage_ms": stage_summary(st2),
+            "roofline": l1_roofline(R2.alg, float(st2[:, 1].mean()), pk),
+            "clocks": c2,
+        }
+        also[name]["roofline"]["traffic"] = None
+        del R2
+        torch.cuda.empty_cache()
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
 
-    pk = peaks()
     l1_ms = float(stage_ms[:, 1].mean())
-    l2_ms = float(stage_ms[:, 2].mean())
-    compute_bound = alg["l1_flops"] / (pk["fp8_tflops"] * 1e12) >= alg["l1_bytes"] / (pk["hbm_gbs"] * 1e9)
-    if compute_bound:
-        achieved = alg["l1_flops"] / (l1_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["fp8_tflops"], "unit": "TFLOP/s"}
-    else:
-        achieved = alg["l1_bytes"] / (l1_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof = l1_roofline(alg, l1_ms, pk)
     roof["traffic"] = traffic_from_profile(kernel_hash(), wl.name, 1.0)
-    roof["kernel"] = "grouped_gemm_kernel<1> (L1 GEMM + SwiGLU/requant epilogue)"
-    roof["peak_source"] = (f"{pk['source']}: MEASURED_PEAKS bf16 burst x2 (FP8-rate block-scaled MMA)"
-                           if compute_bound else f"{pk['source']}: MEASURED_PEAKS hbm_gbs")
-    t_roof = max(alg["flops"] / (pk["fp8_tflops"] * 1e12), alg["bytes"] / (pk["hbm_gbs"] * 1e9))
+    t_roof = step_roofline_time(alg, pk)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
@@ -494,14 +572,13 @@ def main():
         "ms_per_step_median": float(np.median(step_ms)), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxf8f6f4 (e4m3 x e2m1, ue8m0/32, fp32 accum, bf16 out)",
         "data": "synthetic (seeded numpy generator; random-init expert weights)",
-        "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k, "tile_n": tile_n,
+        "config": {"workload": wl.name, "T": T, "H": H, "I": wl.I, "E": wl.E, "k": k, "tile_n": R.tile_n,
                    "l2": "flushed between steps (256 MiB write outside the timed intervals)",
                    "touched_experts": alg["touched"]},
         "tflops": alg["flops"] / (ms_per_step / 1e3) / 1e12 * world,
         "hbm_gbs": alg["bytes"] / (ms_per_step / 1e3) / 1e9,
         "roofline_step_frac": t_roof / (ms_per_step / 1e3),
-        "stage_ms": {"tables+gather": float(stage_ms[:, 0].mean()), "l1_gemm": l1_ms, "l2_gemm": l2_ms,
-                     "combine": float(stage_ms[:, 3].mean())},
+        "stage_ms": stage_summary(stage_ms),
         "roofline": roof,
         "e2e": {"value": whole_job_rate(T * K, world, e2e_pipe_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -511,7 +588,9 @@ def main():
         "gpu_launches": KERNELS_PER_STEP * K,
         "wall_s": wall,
     }
-    line["clocks"] = clocks.summary()
+    line["clocks"] = clock_summary
+    if also:
+        line["per_workload"] = also
     if not args.no_cpu_baseline and world == 1:
         import oracle
         ridx, rw = oracle.route(inp["logits"], k)

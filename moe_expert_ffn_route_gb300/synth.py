@@ -72,6 +72,11 @@ WORKLOADS: Dict[str, Workload] = {
     "prefill": Workload("prefill", 8192, 7168, 2048, 256, 8, 3),
     "skewed": Workload("skewed", 4000, 7168, 2048, 256, 8, 4, routing="zipf",
                        zipf_s=1.2, n_cold=24, outlier_frac=0.01, outlier_scale=64.0),
+    # the prefill and decode shapes at E = 32: the same rows per expert (256 and
+    # 4), so the same token tiles and per-tile work, with 1/8 of the weights;
+    # small enough for hardware-counter captures of single GEMM launches
+    "prefill_e32": Workload("prefill_e32", 1024, 7168, 2048, 32, 8, 5),
+    "decode_e32": Workload("decode_e32", 16, 7168, 2048, 32, 8, 6),
 }
 
 
