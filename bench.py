@@ -40,7 +40,7 @@ METRIC = "fused MoE fwd tokens/s & TFLOP/s, % of roofline (1×GB300)"
 DEFAULT_WORKLOAD = "prefill"          # the largest single-GPU configuration (compute-bound)
 ALSO_TIMED = ("decode",)              # timed after the headline in the same run (weight-streaming)
 L2_BYTES = 129 * 1024 * 1024
-KERNELS_PER_STEP = 6      # route, layout count, dispatch/gather, L1 GEMM, L2 GEMM, combine
+KERNELS_PER_STEP = 5      # route, layout count, dispatch/gather, grouped GEMM (L1 + L2), combine
 
 
 def peaks():
@@ -330,6 +330,8 @@ class DeviceRun:
         self.inp = synth.make_inputs(wl)
         T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
         self.prob = mb.problem(T, H, I, E, k)
+        # the same forward with the two layers as two launches (per-layer times)
+        self.prob_split = mb.problem(T, H, I, E, k, debug_flags=mb.DEBUG_SPLIT_LAYERS)
         self.tile_n = mb.tile_n(self.prob)
 
         def up(a):
@@ -349,18 +351,19 @@ class DeviceRun:
         self.flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
         self.stream = torch.cuda.current_stream()
 
-    def step(self, events=None, logits=None, x=None, x_sf=None, y=None):
+    def step(self, events=None, logits=None, x=None, x_sf=None, y=None, split=False):
         """One pass of the whole hot path: routing, then the fused forward."""
         mb, k = self.mb, self.wl.k
         logits = self.logits if logits is None else logits
         x = self.x if x is None else x
         x_sf = self.x_sf if x_sf is None else x_sf
         y = self.y if y is None else y
+        prob = self.prob_split if split else self.prob
         mb.route_topk(logits, k, self.idx, self.wts)
         if events is None:
-            mb.forward(self.prob, x, x_sf, self.idx, self.wts, self.prepared, self.ws, y)
+            mb.forward(prob, x, x_sf, self.idx, self.wts, self.prepared, self.ws, y)
         else:
-            mb.forward_profiled(self.prob, x, x_sf, self.idx, self.wts, self.prepared, self.ws, y, events)
+            mb.forward_profiled(prob, x, x_sf, self.idx, self.wts, self.prepared, self.ws, y, events)
 
     def warm(self, W):
         import torch
@@ -396,28 +399,34 @@ class DeviceRun:
         step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
         # per-stage times from separate steps with events between the stages (the
         # events keep one kernel from starting before the previous one ends, so
-        # these steps are not the timed ones)
+        # these steps are not the timed ones); then the same with the two layers
+        # as two launches, for per-layer times
         KP = min(K, 20)
-        stages = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(KP)]
-        for i in range(KP):
-            self.step(stages[i])
-            self.flush.fill_(i & 0xFF)
-        torch.cuda.synchronize()
-        stage_ms = np.array([[ev[j].elapsed_time(ev[j + 1]) for j in range(4)] for ev in stages])
+        stage_ms = []
+        for split in (False, True):
+            stages = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(KP)]
+            for i in range(KP):
+                self.step(stages[i], split=split)
+                self.flush.fill_(i & 0xFF)
+            torch.cuda.synchronize()
+            stage_ms.append(np.array([[ev[j].elapsed_time(ev[j + 1]) for j in range(4)] for ev in stages]))
         return step_ms, stage_ms, clocks.summary(), wall
 
 
-def l1_roofline(alg, l1_ms, pk):
-    """The L1 GEMM launch against the bound its arithmetic intensity sets."""
-    compute_bound = alg["l1_flops"] / (pk["fp8_tflops"] * 1e12) >= alg["l1_bytes"] / (pk["hbm_gbs"] * 1e9)
+def gemm_roofline(alg, gemm_ms, pk):
+    """The grouped-GEMM launch (L1 and L2 items) against the bound its
+    arithmetic intensity sets."""
+    flops = alg["l1_flops"] + alg["l2_flops"]
+    nbytes = alg["l1_bytes"] + alg["l2_bytes"]
+    compute_bound = flops / (pk["fp8_tflops"] * 1e12) >= nbytes / (pk["hbm_gbs"] * 1e9)
     if compute_bound:
-        achieved = alg["l1_flops"] / (l1_ms / 1e3) / 1e12
+        achieved = flops / (gemm_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["fp8_tflops"], "unit": "TFLOP/s"}
     else:
-        achieved = alg["l1_bytes"] / (l1_ms / 1e3) / 1e9
+        achieved = nbytes / (gemm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = "grouped_gemm_kernel<1> (L1 GEMM + SwiGLU/requant epilogue)"
+    roof["kernel"] = "grouped_gemm_kernel (L1 items with the SwiGLU/requant epilogue, then L2 items; one launch)"
     roof["peak_source"] = (f"{pk['source']}: MEASURED_PEAKS bf16 burst x2 (FP8-rate block-scaled MMA)"
                            if compute_bound else f"{pk['source']}: MEASURED_PEAKS hbm_gbs")
     return roof
@@ -428,8 +437,16 @@ def step_roofline_time(alg, pk):
 
 
 def stage_summary(stage_ms):
-    return {"tables+gather": float(stage_ms[:, 0].mean()), "l1_gemm": float(stage_ms[:, 1].mean()),
-            "l2_gemm": float(stage_ms[:, 2].mean()), "combine": float(stage_ms[:, 3].mean())}
+    """Stage means of the one-launch forward, and the layer times of the
+    two-launch form of the same forward."""
+    one, two = stage_ms
+    return {"tables+gather": float(one[:, 0].mean()), "grouped_gemm": float(one[:, 1:3].sum(axis=1).mean()),
+            "combine": float(one[:, 3].mean()),
+            "two_launches": {"l1_gemm": float(two[:, 1].mean()), "l2_gemm": float(two[:, 2].mean())}}
+
+
+def gemm_ms_of(stage_ms):
+    return float(stage_ms[0][:, 1:3].sum(axis=1).mean())
 
 
 def main():
@@ -549,7 +566,7 @@ def main():
             "hbm_gbs": R2.alg["bytes"] / (ms2 / 1e3) / 1e9,
             "roofline_step_frac": step_roofline_time(R2.alg, pk) / (ms2 / 1e3),
             "stage_ms": stage_summary(st2),
-            "roofline": l1_roofline(R2.alg, float(st2[:, 1].mean()), pk),
+            "roofline": gemm_roofline(R2.alg, gemm_ms_of(st2), pk),
             "clocks": c2,
         }
         also[name]["roofline"]["traffic"] = None
@@ -561,8 +578,7 @@ def main():
             torch.distributed.destroy_process_group()
         return
 
-    l1_ms = float(stage_ms[:, 1].mean())
-    roof = l1_roofline(alg, l1_ms, pk)
+    roof = gemm_roofline(alg, gemm_ms_of(stage_ms), pk)
     roof["traffic"] = traffic_from_profile(kernel_hash(), wl.name, 1.0)
     t_roof = step_roofline_time(alg, pk)
 

@@ -88,7 +88,11 @@ typedef void* moeffn_stream;
  *   bit 1 (MOEFFN_DEBUG_DUMP_L1_ACC): the forward stops after the L1 GEMM
  *     and leaves its raw FP32 accumulators in the output-pool view as
  *     float [P_max][2I] (gate channels 0..I-1, then up channels); needs
- *     4*I <= H, else MOEFFN_ERR_UNSUPPORTED; y is not written.
+ *     4*I <= H, else MOEFFN_ERR_UNSUPPORTED; y is not written;
+ *   bit 2 (MOEFFN_DEBUG_SPLIT_LAYERS): the grouped GEMM runs as two
+ *     launches, all L1 items and then all L2 items, instead of one launch
+ *     in which each L2 item waits for its token tile's L1 items; the
+ *     results are the same bit for bit (per-layer timing, tests).
  * Pointers: x and y 16-byte aligned; prepared and workspace 256-byte
  * aligned; other arrays aligned to their element size (INVALID_ARG). */
 typedef struct moeffn_problem {
@@ -106,6 +110,7 @@ typedef struct moeffn_problem {
 
 #define MOEFFN_DEBUG_STARVE_L1 1
 #define MOEFFN_DEBUG_DUMP_L1_ACC 2
+#define MOEFFN_DEBUG_SPLIT_LAYERS 4
 
 /* Views into a workspace after moeffn_forward (for inspection and tests).
  * P_max = align(T*min(k,E) + E*127, 128) pool rows; P = offsets[E] <= P_max
@@ -173,7 +178,9 @@ MOEFFN_API moeffn_status moeffn_prepare_weights(const moeffn_problem* problem,
 /* Top-k routing (MegaMoE notes "Problem background": the router picks the
  * top-k experts of each token; the configs define it as softmax over the
  * router logits, top-k, weights renormalised over the selected experts).
- *   logits      float [T][E]; must not contain NaN; -inf allowed
+ *   logits      float [T][E]; -inf allowed; a NaN logit ranks below every
+ *               number (the pages leave NaN undefined; this is the reading
+ *               the oracle follows too), so every id is valid and distinct
  *   topk_idx    int64 [T][k] out: experts by descending logit, ties to the
  *               lower expert index
  *   topk_w      float [T][k] out: exp(l_j - l_1) / sum_selected exp(l - l_1)
@@ -195,6 +202,13 @@ MOEFFN_API moeffn_status moeffn_route_topk(const float* logits, int32_t num_toke
  *              accumulated in FP32 in j order, rounded to BF16 (RNE)
  * Errors: see the conventions above; workspace_bytes too small ->
  * WORKSPACE_TOO_SMALL.  T = 0 launches nothing.
+ * Kernels: schedule tables, gather, ONE persistent grouped-GEMM launch (the
+ * L1 items, then the L2 items, each L2 item waiting for the L1 items of its
+ * token tile through GPU-scope counters: MegaMoE notes, "L1 -> L2
+ * dependencies"), combine.  The GEMM launch sizes its grid to the CTA pairs
+ * that can be resident at once and needs all of them resident together:
+ * run the forward with the GPU to itself (another kernel holding SMs for
+ * seconds would make the L2 items' bounded waits report a timeout).
  * On `stream` the call only launches kernels (the host checks arguments and
  * encodes tensor maps), so moeffn_route_topk and moeffn_forward can be
  * captured in a CUDA graph; a replay recomputes from what the buffers hold
@@ -209,6 +223,8 @@ MOEFFN_API moeffn_status moeffn_forward(const moeffn_problem* problem,
  * (cudaEvent_t handles, same device) on `stream` at the stage boundaries:
  *   stage_events[0] before the schedule tables, [1] after the gather,
  *   [2] after the L1 GEMM, [3] after the L2 GEMM, [4] after the combine.
+ *   The two layers run in one launch unless MOEFFN_DEBUG_SPLIT_LAYERS is
+ *   set, so [2] and [3] are then recorded at the same point (after both).
  * Lets a caller time each stage with cudaEventElapsedTime.  A NULL array
  * or handle -> INVALID_ARG; otherwise errors as moeffn_forward. */
 MOEFFN_API moeffn_status moeffn_forward_profiled(const moeffn_problem* problem,
@@ -230,7 +246,8 @@ MOEFFN_API moeffn_status moeffn_query(const moeffn_problem* problem, void* works
  * Word [1] names the first wait that ran out: 1 a TMA producer (stage free),
  * 2 an MMA warp (accumulator drained), 3 an MMA warp (stage loaded),
  * 4 the epilogue (accumulator ready), 5 and 6 the end-of-kernel drains of
- * copies and MMAs.  With a whole grid waiting on one failure, which of them
+ * copies and MMAs, 7 a TMA producer waiting for the L1 rows of an L2 item's
+ * token tile.  With a whole grid waiting on one failure, which of them
  * expires first is a race. */
 MOEFFN_API moeffn_status moeffn_get_device_status(const moeffn_problem* problem, void* workspace,
                                        moeffn_stream stream, uint32_t* detail);

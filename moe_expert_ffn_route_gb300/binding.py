@@ -38,6 +38,7 @@ STATUS = {0: "MOEFFN_OK", 1: "MOEFFN_ERR_INVALID_ARG", 2: "MOEFFN_ERR_UNSUPPORTE
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_TIMEOUT = range(6)
 DEBUG_STARVE_L1 = 1
 DEBUG_DUMP_L1_ACC = 2
+DEBUG_SPLIT_LAYERS = 4
 
 VIEWS = {"status": 0, "counts": 1, "offsets": 2, "tiles": 3, "slots": 4, "row2tk": 5, "wpool": 6,
          "slack": 7, "xpool": 8, "xpool_sf": 9, "hpool": 10, "hpool_sf": 11, "ypool": 12,

@@ -22,7 +22,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct WsLayout {
-    size_t status, counts, offsets, tiles, tile_rows, tile_rec, slots, rank, hist, row2tk, wpool, slack;
+    size_t status, counts, offsets, tiles, tile_rows, tile_rec, l1_done, slots, rank, hist, row2tk, wpool, slack;
     size_t xpool, xpool_sf, hpool, hpool_sf, ypool, total;
     int64_t P_max, NT_max, nchunks;
 };
@@ -40,7 +40,8 @@ moeffn_status check_problem(const moeffn_problem* p) {
     if (p->tile_n != 0 && (p->tile_n % kTileQuantum != 0 || p->tile_n < 32 || p->tile_n > kMaxTileN))
         return MOEFFN_ERR_INVALID_ARG;
     if (p->wait_timeout_us < 0) return MOEFFN_ERR_INVALID_ARG;
-    if (p->debug_flags & ~(MOEFFN_DEBUG_STARVE_L1 | MOEFFN_DEBUG_DUMP_L1_ACC)) return MOEFFN_ERR_INVALID_ARG;
+    if (p->debug_flags & ~(MOEFFN_DEBUG_STARVE_L1 | MOEFFN_DEBUG_DUMP_L1_ACC | MOEFFN_DEBUG_SPLIT_LAYERS))
+        return MOEFFN_ERR_INVALID_ARG;
     if ((p->debug_flags & MOEFFN_DEBUG_DUMP_L1_ACC) && 4 * p->intermediate > p->hidden)
         return MOEFFN_ERR_UNSUPPORTED;
     if (!(p->act_clamp <= 0.f || p->act_clamp > 0.f)) return MOEFFN_ERR_INVALID_ARG;   // NaN
@@ -87,6 +88,7 @@ WsLayout ws_layout(const moeffn_problem& p) {
     L.tiles = take(4 * (E + 1));
     L.tile_rows = take(4 * E);
     L.tile_rec = take(32 * L.NT_max);
+    L.l1_done = take(4 * L.NT_max);
     L.slots = take(4 * N);
     L.rank = take(4 * N);
     L.hist = take(4 * L.nchunks * E);
@@ -293,9 +295,10 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
     int* tile_rec = reinterpret_cast<int*>(w + L.tile_rec);
     int* slots = reinterpret_cast<int*>(w + L.slots);
 
+    int* l1_done = reinterpret_cast<int*>(w + L.l1_done);
     LayoutArgs la{x, x_sf, topk_idx, topk_w, T, H, E, k, tile_n,
                   reinterpret_cast<int*>(w + L.hist), reinterpret_cast<int*>(w + L.rank), counts, offsets,
-                  tiles, tile_rows, tile_rec, slots, reinterpret_cast<int*>(w + L.row2tk), reinterpret_cast<float*>(w + L.wpool),
+                  tiles, tile_rows, tile_rec, l1_done, slots, reinterpret_cast<int*>(w + L.row2tk), reinterpret_cast<float*>(w + L.wpool),
                   reinterpret_cast<int*>(w + L.slack), w + L.xpool, reinterpret_cast<uint32_t*>(w + L.xpool_sf),
                   status};
     if (launch_layout(la, st) != cudaSuccess || !mark(1)) return MOEFFN_ERR_CUDA;
@@ -336,9 +339,27 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
     g.num_sms = num_sms;
     g.tile_n = tile_n;
 
-    if (launch_gemm(1, m1, g, st) != cudaSuccess || !mark(2)) return MOEFFN_ERR_CUDA;
-    if (p->debug_flags & MOEFFN_DEBUG_DUMP_L1_ACC) return MOEFFN_OK;   // accumulators left in the output pool
-    if (launch_gemm(2, m2, g, st) != cudaSuccess || !mark(3)) return MOEFFN_ERR_CUDA;
+    g.l1_done = l1_done;
+    if (p->debug_flags & MOEFFN_DEBUG_DUMP_L1_ACC) {
+        // L1 only: the raw accumulators are left in the output pool
+        g.run_l1 = 1;
+        g.run_l2 = 0;
+        return launch_gemm(m1, m2, g, st) == cudaSuccess && mark(2) ? MOEFFN_OK : MOEFFN_ERR_CUDA;
+    }
+    if (p->debug_flags & MOEFFN_DEBUG_SPLIT_LAYERS) {
+        // the two layers as two launches of the same kernel (the stream orders them)
+        g.run_l1 = 1;
+        g.run_l2 = 0;
+        if (launch_gemm(m1, m2, g, st) != cudaSuccess || !mark(2)) return MOEFFN_ERR_CUDA;
+        g.run_l1 = 0;
+        g.run_l2 = 1;
+        if (launch_gemm(m1, m2, g, st) != cudaSuccess || !mark(3)) return MOEFFN_ERR_CUDA;
+    } else {
+        // one persistent launch: every L2 item waits for the L1 items of its token tile
+        g.run_l1 = 1;
+        g.run_l2 = 1;
+        if (launch_gemm(m1, m2, g, st) != cudaSuccess || !mark(2) || !mark(3)) return MOEFFN_ERR_CUDA;
+    }
 
     if (launch_combine(reinterpret_cast<const uint16_t*>(w + L.ypool), slots, T, H, k, y, st) != cudaSuccess ||
         !mark(4))

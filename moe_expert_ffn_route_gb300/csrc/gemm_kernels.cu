@@ -162,6 +162,67 @@ __device__ __forceinline__ TileInfo decode_rec(int t, int ncb, const TileRec& r)
     return ti;
 }
 
+// The tensor maps of one layer (kernel parameters).
+struct LayerMaps {
+    CUtensorMap a;      // prepared weights, boxes of 128 rows x 128 K
+    CUtensorMap sfa;    // weight scales, one 512-B row per box
+    CUtensorMap sfb;    // pool scales, one row (512 B or 1 KB) per box
+    TokenMaps b;        // token pool, boxes of 8 .. kMaxTileN / 2 rows
+};
+
+// The items of one launch: n1 L1 items (indices [0, n1)) then n2 L2 items.
+// Within a layer, item u covers token tile u / ncb and weight block u % ncb
+// of that tile's expert (see decode_rec).
+struct Sched {
+    int n1, n;                 // L1 items, all items
+    int ncb1, ncb2;            // 256-row weight blocks per expert (W1: 2I rows, W2: H rows)
+    int nkb1, nkb2;            // 128-wide K blocks (L1: H, L2: I)
+    int rows1, rows2;          // weight rows per expert
+    __device__ __forceinline__ int ncb(int layer) const { return layer == 1 ? ncb1 : ncb2; }
+    __device__ __forceinline__ int nkb(int layer) const { return layer == 1 ? nkb1 : nkb2; }
+    __device__ __forceinline__ int rows(int layer) const { return layer == 1 ? rows1 : rows2; }
+};
+__device__ __forceinline__ int item_layer(int t, const Sched& s) { return t < s.n1 ? 1 : 2; }
+__device__ __forceinline__ int item_local(int t, const Sched& s) { return t < s.n1 ? t : t - s.n1; }
+__device__ __forceinline__ TileRec item_rec(int t, const Sched& s, const GemmArgs& p) {
+    return load_rec(item_local(t, s), s.ncb(item_layer(t, s)), p);
+}
+__device__ __forceinline__ TileInfo item_info(int t, const Sched& s, const TileRec& r) {
+    return decode_rec(item_local(t, s), s.ncb(item_layer(t, s)), r);
+}
+
+// Wait, bounded, until every L1 item of a token tile has published its rows:
+// one lane polls the tile's counter with acquire loads at GPU scope; on
+// success the warp orders its later asynchronous-proxy reads (TMA loads of
+// those rows) after the rows the counter published.
+__device__ __forceinline__ bool wait_l1_rows(const int* ctr, int target, volatile int* abort, uint64_t timeout_ns,
+                                             DevStatus* st) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v < target) {
+            const uint64_t t0 = global_timer_ns();
+            while (true) {
+                __nanosleep(64);
+                asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+                if (v >= target) break;
+                if (*abort) { ok = 0; break; }
+                if (global_timer_ns() - t0 > timeout_ns) {
+                    atomicOr(&st->code, DEV_ERR_TIMEOUT);
+                    atomicCAS(&st->detail, 0u, 7u);
+                    *abort = 1;
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) asm volatile("fence.proxy.async.global;" ::: "memory");
+    return ok != 0;
+}
+
 // the 64 threads of gate/up warp pair pi = 2 * group + pair (warps 2 pi, 2 pi + 1)
 __device__ __forceinline__ void pair_sync(int pi) {
     switch (pi) {
@@ -174,10 +235,9 @@ __device__ __forceinline__ void pair_sync(int pi) {
     }
 }
 
-template <int LAYER, int BN, int RW>
+template <int BN, int RW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, RW>::THREADS, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TokenMaps tmB,
-                    const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant__ LayerMaps m2,
                     const GemmArgs p) {
     using C = GemmCfg<BN, RW>;
     constexpr int S = C::STAGES, ACC = C::NACC;
@@ -215,10 +275,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         mbar_init(mma_done, kMmaWarps);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmSFA);
-        prefetch_tensormap(&tmSFB);
-        for (int i = 0; i < kNumTokenBoxes; ++i) prefetch_tensormap(&tmB.m[i]);
+        prefetch_tensormap(&m1.a);
+        prefetch_tensormap(&m1.sfa);
+        prefetch_tensormap(&m1.sfb);
+        prefetch_tensormap(&m2.a);
+        prefetch_tensormap(&m2.sfa);
+        prefetch_tensormap(&m2.sfb);
     }
     if (warp == kFirstMmaWarp) {
         tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -233,10 +295,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     pdl_launch_dependents();
 
     const int npairs = gridDim.x >> 1, pair = blockIdx.x >> 1;
-    const int ncb = LAYER == 1 ? p.I / 128 : (p.H + 255) / 256;   // 256-row weight tiles (pairs) per expert
-    const int nkb = LAYER == 1 ? p.H / 128 : p.I / 128;           // 128-wide K blocks
-    const int a_rows = LAYER == 1 ? 2 * p.I : p.H;                 // weight rows per expert
-    const int total = __ldg(p.tiles + p.E) * ncb;
+    Sched sc;
+    sc.ncb1 = p.I / 128;
+    sc.ncb2 = (p.H + 255) / 256;
+    sc.nkb1 = p.H / 128;
+    sc.nkb2 = p.I / 128;
+    sc.rows1 = 2 * p.I;
+    sc.rows2 = p.H;
+    {
+        const int tiles = __ldg(p.tiles + p.E);
+        sc.n1 = p.run_l1 ? tiles * sc.ncb1 : 0;
+        sc.n = sc.n1 + (p.run_l2 ? tiles * sc.ncb2 : 0);
+    }
+    const int total = sc.n;
+    // an L2 item in the same launch as the L1 items waits for its token tile's rows
+    const bool wait_l1 = sc.n1 > 0;
+    const int l1_target = 2 * kEpiWarps * sc.ncb1;    // one count per epilogue warp of both CTAs per L1 item
 
     if (warp >= kFirstProducerWarp) {
         // ------------------------------------------------------------ TMA (both CTAs)
@@ -250,13 +324,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int ls = 0;                                  // stage within the ring
             uint32_t phase = 0;
             uint32_t armed[C::RING] = {};
-            const bool starve = LAYER == 1 && (p.debug_flags & 1) && rank == 0 && ring == 0;
+            const bool starve = (p.debug_flags & 1) && rank == 0 && ring == 0;
             bool ok = true;
             const int t_first = pair + ring * npairs;
-            TileRec rec = t_first < total ? load_rec(t_first, ncb, p) : TileRec{};
+            TileRec rec = t_first < total ? item_rec(t_first, sc, p) : TileRec{};
             for (int t = t_first; t < total && ok; t += 2 * npairs) {
-                const TileInfo ti = decode_rec(t, ncb, rec);
-                if (t + 2 * npairs < total) rec = load_rec(t + 2 * npairs, ncb, p);
+                const TileInfo ti = item_info(t, sc, rec);
+                const int layer = item_layer(t, sc);
+                const LayerMaps& m = layer == 1 ? m1 : m2;
+                const int nkb = sc.nkb(layer), a_rows = sc.rows(layer);
+                if (t + 2 * npairs < total) rec = item_rec(t + 2 * npairs, sc, p);
+                if (layer == 2 && wait_l1 &&
+                    !wait_l1_rows(p.l1_done + ti.tile_idx, l1_target, abort_flag, p.timeout_ns, p.status)) {
+                    ok = false;
+                    break;
+                }
                 const int mrow = ti.cb * 256 + 128 * static_cast<int>(rank);   // first weight row of this CTA
                 const bool mine_valid = mrow < a_rows;                          // false only for an L2 tail half
                 const int a0 = ti.e * a_rows + mrow;
@@ -265,7 +347,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int sfb_row = ti.tile_idx * nkb;       // rows of 1 KB: one per token tile and K block
                 const int half = ti.ncols / 2;
                 const int box = box_for_half(half);
-                const CUtensorMap* tmBox = &tmB.m[box];
+                const CUtensorMap* tmBox = &m.b.m[box];
                 const int brow = ti.row0 + half * static_cast<int>(rank);
                 const uint32_t bytes = C::A_TX_BYTES + box_half_rows(box) * 128 + 512 + C::SFB_BYTES;
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -284,13 +366,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     const uint32_t sb = sbase + stage * C::STAGE_BYTES;
                     const uint32_t ss = sfbase + stage * C::SF_STAGE;
-                    if (!(starve && t == pair && kb == 0)) {
+                    if (!(starve && t == pair && layer == 1 && kb == 0)) {
                         const uint32_t fb = leader_full0 + 8u * stage;
                         if (rank == 0) mbar_arrive_expect_tx_w(full(stage), 2 * bytes);
-                        tma_load_2d_pair_w(sb, &tmA, fb, kb * 128, a0);
+                        tma_load_2d_pair_w(sb, &m.a, fb, kb * 128, a0);
                         tma_load_2d_pair_w(sb + C::A_BYTES, tmBox, fb, kb * 128, brow);
-                        tma_load_2d_pair_w(ss, &tmSFA, fb, 0, sfa_row + kb);
-                        tma_load_2d_pair_w(ss + 512, &tmSFB, fb, 0, sfb_row + kb);
+                        tma_load_2d_pair_w(ss, &m.sfa, fb, 0, sfa_row + kb);
+                        tma_load_2d_pair_w(ss + 512, &m.sfb, fb, 0, sfb_row + kb);
                         ++armed[ls];
                     }
                     if (++ls == C::RING) {
@@ -324,10 +406,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             bool ok = true;
             const uint32_t sf_base = tmem + C::SF_COL + static_cast<uint32_t>(ring * 2 * C::SF_SET_COLS);
             const int t_first = pair + ring * npairs;
-            TileRec rec = t_first < total ? load_rec(t_first, ncb, p) : TileRec{};
+            TileRec rec = t_first < total ? item_rec(t_first, sc, p) : TileRec{};
             for (int t = t_first; t < total && ok; t += 2 * npairs, ++it) {
-                const TileInfo ti = decode_rec(t, ncb, rec);
-                if (t + 2 * npairs < total) rec = load_rec(t + 2 * npairs, ncb, p);
+                const TileInfo ti = item_info(t, sc, rec);
+                const int nkb = sc.nkb(item_layer(t, sc));
+                if (t + 2 * npairs < total) rec = item_rec(t + 2 * npairs, sc, p);
                 const uint32_t idesc_n = IDESC | (static_cast<uint32_t>(ti.ncols >> 3) << 17);
                 const bool two_sfb = ti.ncols > 128;
                 const int tord = 2 * it + ring;                // ordinal of this tile in the pair's sequence
@@ -384,15 +467,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
         const uint32_t leader_tempty0 = map_shared_rank(tempty(0), 0);
         int it = 0;
-        TileRec rec = pair < total ? load_rec(pair, ncb, p) : TileRec{};
+        TileRec rec = pair < total ? item_rec(pair, sc, p) : TileRec{};
         for (int t = pair; t < total; t += npairs, ++it) {
-            const TileInfo ti = decode_rec(t, ncb, rec);
-            if (t + npairs < total) rec = load_rec(t + npairs, ncb, p);
+            const TileInfo ti = item_info(t, sc, rec);
+            const bool l1 = item_layer(t, sc) == 1;
+            if (t + npairs < total) rec = item_rec(t + npairs, sc, p);
             const int as = it % ACC;
             const uint32_t ap = static_cast<uint32_t>(it / ACC) & 1u;
             const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(tfull(as), ap, abort_flag, p.timeout_ns,
                                                                         p.status, 4));
-            if constexpr (LAYER == 1) {
+            if (l1) {
                 // the two warps of a gate/up pair meet at named barriers below, so
                 // they decide together whether to go on (a timeout may reach only one)
                 const int pi = warp >> 1, hs = q & 1;
@@ -408,7 +492,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t tacc = tq + static_cast<uint32_t>(as * RW);
             const int nchunks = (ti.nvalid + 31) / 32;
             const int mrow = ti.cb * 256 + 128 * static_cast<int>(rank);
-            if constexpr (LAYER == 1) {
+            if (l1) {
                 // Quarter q holds band q of this CTA's 128 rows: gate (q even) or up
                 // (q odd) of channels cbase + [0, 32), cbase = mrow / 2 + 32 (q / 2);
                 // thread `lane` has channel cbase + lane for the chunk's 32 tokens.
@@ -564,6 +648,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             // complete (tcgen05.wait::ld) and fenced above; the rows stored to global
             // memory are not read by that warp, and a release would wait for them
             if (lane == 0) mbar_arrive_remote_relaxed(leader_tempty0 + 8u * as);
+            if (l1 && wait_l1) {
+                // publish this warp's share of the token tile's L1 rows and scales to
+                // the L2 items of the same launch, which read them by TMA (the
+                // asynchronous proxy): proxy fence, GPU-scope fence, then one count
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(p.l1_done + ti.tile_idx, 1);
+            }
         }
     }
 
@@ -576,13 +669,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
 }
 
-template <int LAYER, int BN, int RW>
-static cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, cudaStream_t stream) {
+template <int BN, int RW>
+static cudaError_t launch_one(const GemmMaps& g1, const GemmMaps& g2, const GemmArgs& a, cudaStream_t stream) {
     using C = GemmCfg<BN, RW>;
-    auto kernel = grouped_gemm_kernel<LAYER, BN, RW>;
+    auto kernel = grouped_gemm_kernel<BN, RW>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (err != cudaSuccess) return err;
-    // persistent grid: as many CTA pairs as can be resident at once
+    // persistent grid: as many CTA pairs as can be resident at once (an L2 item
+    // waits for L1 items of other pairs, so all pairs must be resident together)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (a.num_sms / 2), 1, 1);
     cfg.blockDim = dim3(C::THREADS, 1, 1);
@@ -599,23 +693,27 @@ static cudaError_t launch_one(const GemmMaps& m, const GemmArgs& a, cudaStream_t
         clusters = a.num_sms / 2;
     }
     cfg.gridDim = dim3(2 * (clusters < a.num_sms / 2 ? clusters : a.num_sms / 2), 1, 1);
-    TokenMaps maps;
-    for (int i = 0; i < kNumTokenBoxes; ++i) maps.m[i] = m.b[i];
-    err = cudaLaunchKernelEx(&cfg, kernel, m.a, maps, m.sfa, BN <= 128 ? m.sfb_512 : m.sfb_1k, a);
+    LayerMaps m1, m2;
+    const GemmMaps* g[2] = {&g1, &g2};
+    LayerMaps* m[2] = {&m1, &m2};
+    for (int l = 0; l < 2; ++l) {
+        m[l]->a = g[l]->a;
+        m[l]->sfa = g[l]->sfa;
+        m[l]->sfb = BN <= 128 ? g[l]->sfb_512 : g[l]->sfb_1k;
+        for (int i = 0; i < kNumTokenBoxes; ++i) m[l]->b.m[i] = g[l]->b[i];
+    }
+    err = cudaLaunchKernelEx(&cfg, kernel, m1, m2, a);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(int layer, const GemmMaps& m, const GemmArgs& a, cudaStream_t stream) {
+cudaError_t launch_gemm(const GemmMaps& m1, const GemmMaps& m2, const GemmArgs& a, cudaStream_t stream) {
     // three stage layouts: tiles of at most 32 rows (10 stages in flight, four
     // accumulator regions), at most 144 rows (8 stages, three regions) and at
     // most kMaxTileN rows (6 stages, two regions)
-    if (a.tile_n <= 32)
-        return layer == 1 ? launch_one<1, 32, 32>(m, a, stream) : launch_one<2, 32, 32>(m, a, stream);
-    if (a.tile_n <= 144)
-        return layer == 1 ? launch_one<1, 144, 144>(m, a, stream) : launch_one<2, 144, 144>(m, a, stream);
-    return layer == 1 ? launch_one<1, kMaxTileN, kMaxTileN>(m, a, stream)
-                      : launch_one<2, kMaxTileN, kMaxTileN>(m, a, stream);
+    if (a.tile_n <= 32) return launch_one<32, 32>(m1, m2, a, stream);
+    if (a.tile_n <= 144) return launch_one<144, 144>(m1, m2, a, stream);
+    return launch_one<kMaxTileN, kMaxTileN>(m1, m2, a, stream);
 }
 
 }  // namespace moeffn

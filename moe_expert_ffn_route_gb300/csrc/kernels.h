@@ -23,6 +23,7 @@ struct LayoutArgs {
     int* tile_rows; // [E]   token rows per tile of each expert (multiple of 16)
     int* tile_rec;  // [NT_max][8] per token tile: expert, its first token tile, its token
                     // tiles, rows per tile, its pool offset, its rows, 0, 0
+    int* l1_done;   // [NT_max] zeroed here: per token tile, L1 epilogue warps done
     int* slots;     // [T*k]
     int* row2tk;    // [P_max]
     float* wpool;   // [P_max]
@@ -62,6 +63,8 @@ struct GemmArgs {
     int fast_math;          // 1: SiLU with approximate exp and reciprocal
     int num_sms;
     int tile_n;             // most token rows per tile (selects the stage layout)
+    int run_l1, run_l2;     // which layers' items this launch runs (L1 items first)
+    int* l1_done;           // [NT_max] per token tile: L1 epilogue warps that published their rows
 };
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int64_t* idx, float* w,
@@ -81,7 +84,9 @@ struct GemmMaps {
     CUtensorMap sfa;
     CUtensorMap sfb_512, sfb_1k;
 };
-// layer = 1 or 2
-cudaError_t launch_gemm(int layer, const GemmMaps& maps, const GemmArgs& a, cudaStream_t stream);
+// One launch of the grouped GEMM kernel over the L1 items (a.run_l1), then
+// the L2 items (a.run_l2): with both, each L2 item waits for the L1 items of
+// its token tile (counters a.l1_done); m1 and m2 are the two layers' maps.
+cudaError_t launch_gemm(const GemmMaps& m1, const GemmMaps& m2, const GemmArgs& a, cudaStream_t stream);
 
 }  // namespace moeffn

@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
     int k, const int* __restrict__ hist, const int* __restrict__ rank,
     const int* __restrict__ counts, const int* __restrict__ offsets,
     const int* __restrict__ tiles, const int* __restrict__ tile_rows, int* __restrict__ tile_rec,
-    int* __restrict__ slots, int* __restrict__ row2tk,
+    int* __restrict__ l1_done, int* __restrict__ slots, int* __restrict__ row2tk,
     float* __restrict__ wpool, int* __restrict__ slack, uint8_t* __restrict__ xpool,
     uint32_t* __restrict__ xpool_sf, int nb_tok) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
             int4* rec = reinterpret_cast<int4*>(tile_rec) + 2 * tt;
             rec[0] = make_int4(e, t0, t1 - t0, tile_rows[e]);
             rec[1] = make_int4(beg, n, 0, 0);
+            l1_done[tt] = 0;    // counts the L1 epilogue warps that published this tile's rows
         }
         for (int r = beg + n + threadIdx.x; r < end; r += blockDim.x) {
             row2tk[r] = -1;
@@ -327,7 +328,7 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
     const int nb_tok = (a.T + tok_per_block - 1) / tok_per_block;
     return launch_pdl(dispatch_kernel, dim3(nb_tok + a.E), dim3(256), 0, stream, a.x, a.x_sf, a.topk_idx,
                       a.topk_w, a.T, a.H, a.E, a.k, a.hist, a.rank, a.counts, a.offsets, a.tiles, a.tile_rows,
-                      a.tile_rec, a.slots, a.row2tk, a.wpool, a.slack, a.xpool, a.xpool_sf, nb_tok);
+                      a.tile_rec, a.l1_done, a.slots, a.row2tk, a.wpool, a.slack, a.xpool, a.xpool_sf, nb_tok);
 }
 
 // ---------------------------------------------------------------------------

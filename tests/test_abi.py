@@ -56,7 +56,8 @@ def test_status_strings():
     (dict(act_clamp=float("nan")), mb.ERR_INVALID_ARG),
     (dict(fast_math=1), mb.OK),
     (dict(fast_math=2), mb.ERR_UNSUPPORTED),
-    (dict(debug_flags=4), mb.ERR_INVALID_ARG),
+    (dict(debug_flags=4), mb.OK),
+    (dict(debug_flags=8), mb.ERR_INVALID_ARG),
     (dict(debug_flags=2, H=1024, I=512), mb.ERR_UNSUPPORTED),
     (dict(debug_flags=2, H=1024, I=256), mb.OK),
     (dict(T=0), mb.OK),
