@@ -218,9 +218,9 @@ def clock_sampler(dev):
 
 
 def traffic_from_profile(kernel_src_hash: str, workload: str, units_scale: float):
-    """DRAM bytes per L1 GEMM launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "l1_gemm_traffic.md")
+    """DRAM bytes per grouped-GEMM launch from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "grouped_gemm_traffic.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -569,7 +569,7 @@ def main():
             "roofline": gemm_roofline(R2.alg, gemm_ms_of(st2), pk),
             "clocks": c2,
         }
-        also[name]["roofline"]["traffic"] = None
+        also[name]["roofline"]["traffic"] = traffic_from_profile(kernel_hash(), name, 1.0)
         del R2
         torch.cuda.empty_cache()
 

@@ -49,11 +49,12 @@ def test_medium_step_model_matches_the_table():
 
 
 def test_traffic_lookup_follows_the_kernel_hash():
-    text = open(os.path.join(ROOT, "profiles", "l1_gemm_traffic.md")).read()
+    text = open(os.path.join(ROOT, "profiles", "grouped_gemm_traffic.md")).read()
     recorded = text.split("kernel source sha256:")[1].split()[0]
-    assert bench.traffic_from_profile(recorded, "medium", 1.0) == 528171520.0
-    assert bench.traffic_from_profile(recorded, "medium", 2.0) == 2 * 528171520.0
-    assert bench.traffic_from_profile("0" * 64, "medium", 1.0) is None     # another kernel source
+    assert bench.traffic_from_profile(recorded, "prefill", 1.0) == 7563061248.0
+    assert bench.traffic_from_profile(recorded, "prefill", 2.0) == 2 * 7563061248.0
+    assert bench.traffic_from_profile(recorded, "decode", 1.0) == 6009995694.0
+    assert bench.traffic_from_profile("0" * 64, "prefill", 1.0) is None     # another kernel source
     assert bench.traffic_from_profile(recorded, "no-such-workload", 1.0) is None
 
 
