@@ -78,7 +78,10 @@ typedef void* moeffn_stream;
  * tile_n: most token rows per grouped-GEMM tile, a multiple of 16 in
  *   [32, 224]; 0 = 32 when T*k/E <= 32, 144 when T*k/E <= 272, else 224.
  *   Each expert's rows are split into ceil(n_e/tile_n) equal tiles rounded
- *   up to 16 rows.
+ *   up to 16 rows.  For tile_n in [48, 144], when T*k > tile_n*E (an
+ *   expert is expected to have more than one tile), that count is rounded
+ *   up to an even number and the grouped GEMM stages each weight tile once
+ *   for two token tiles of its expert (moeffn_paired_tiles).
  * wait_timeout_us: limit of every bounded device wait in microseconds;
  *   0 = 2 000 000 (2 s).
  * debug_flags: 0 for normal use.  Test hooks:
@@ -114,7 +117,8 @@ typedef struct moeffn_problem {
 
 /* Views into a workspace after moeffn_forward (for inspection and tests).
  * P_max = align(T*min(k,E) + E*127, 128) pool rows; P = offsets[E] <= P_max
- * rows are in use; NT_max = ceil(T*k/tile_n) + E token tiles.  The n-th tile
+ * rows are in use; NT_max = ceil(T*k/tile_n) + E token tiles (+ 2E when
+ * tiles are paired).  The n-th tile
  * of expert e has index tiles[e] + n and covers pool rows offsets[e] +
  * n*tile_rows[e] onwards.  Pool scale factors are stored per token tile and
  * per 128-wide K block as 256 uint32 words: word 128*h + 4*l + c holds the
@@ -147,6 +151,11 @@ MOEFFN_API moeffn_status moeffn_check_problem(const moeffn_problem* problem);
 
 /* Token tile rows the forward will use for this problem (host only). */
 MOEFFN_API moeffn_status moeffn_tile_n(const moeffn_problem* problem, int32_t* tile_n);
+
+/* 1 when the forward splits every expert into an even number of token tiles
+ * whose pairs share each weight stage of the grouped GEMM, else 0 (host
+ * only; the rule is under tile_n above). */
+MOEFFN_API moeffn_status moeffn_paired_tiles(const moeffn_problem* problem, int32_t* paired);
 
 /* Bytes of device workspace moeffn_forward needs (host only).  It holds the
  * schedule tables, the expert-sorted L1/L2 pools and their scales, and the

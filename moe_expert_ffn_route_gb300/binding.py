@@ -50,6 +50,7 @@ SIGNATURES = {
     "moeffn_abi_version": (c_int32, []),
     "moeffn_check_problem": (c_int32, [ctypes.POINTER(Problem)]),
     "moeffn_tile_n": (c_int32, [ctypes.POINTER(Problem), ctypes.POINTER(c_int32)]),
+    "moeffn_paired_tiles": (c_int32, [ctypes.POINTER(Problem), ctypes.POINTER(c_int32)]),
     "moeffn_workspace_bytes": (c_int32, [ctypes.POINTER(Problem), ctypes.POINTER(c_size_t)]),
     "moeffn_prepared_weight_bytes": (c_int32, [ctypes.POINTER(Problem), ctypes.POINTER(c_size_t)]),
     "moeffn_prepare_weights": (c_int32, [ctypes.POINTER(Problem), c_void_p, c_void_p, c_void_p, c_void_p,
@@ -117,6 +118,12 @@ def tile_n(prob: Problem) -> int:
     v = c_int32()
     _check(load().moeffn_tile_n(ctypes.byref(prob), ctypes.byref(v)), "moeffn_tile_n")
     return v.value
+
+
+def paired_tiles(prob: Problem) -> bool:
+    v = c_int32()
+    _check(load().moeffn_paired_tiles(ctypes.byref(prob), ctypes.byref(v)), "moeffn_paired_tiles")
+    return v.value == 1
 
 
 def workspace_bytes(prob: Problem) -> int:

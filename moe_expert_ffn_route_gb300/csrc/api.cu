@@ -67,6 +67,17 @@ int choose_tile_n(const moeffn_problem& p) {
     return m <= 32.0 ? 32 : m <= 272.0 ? 144 : kMaxTileN;
 }
 
+// Pairs of token tiles per weight stage (tile bounds of 48 to 144 rows) when
+// an expert is expected to have more than one tile, T*k > tile_n*E: then each
+// weight stage feeds two tiles of its expert.  With fewer rows per expert
+// most experts would get two half tiles sharing one weight stream, where one
+// tile per stage keeps two weight streams per SM pair in flight.
+bool choose_paired(const moeffn_problem& p) {
+    const int tile_n = choose_tile_n(p);
+    return pairable_tile_n(tile_n) &&
+           static_cast<int64_t>(p.num_tokens) * p.topk > static_cast<int64_t>(tile_n) * p.num_experts;
+}
+
 WsLayout ws_layout(const moeffn_problem& p) {
     WsLayout L{};
     const int64_t T = p.num_tokens, H = p.hidden, I = p.intermediate, E = p.num_experts, k = p.topk;
@@ -74,7 +85,9 @@ WsLayout ws_layout(const moeffn_problem& p) {
     const int64_t kmin = k < E ? k : E;
     L.P_max = static_cast<int64_t>(align_up(static_cast<size_t>(T * kmin + E * (kPoolBlock - 1)), kPoolBlock));
     const int64_t bn = choose_tile_n(p);
-    L.NT_max = (N + bn - 1) / bn + E;
+    // ceil(n_e / bn) tiles per expert, rounded up to even when paired: fewer
+    // than n_e / bn + 1 (+ 2 when paired) per expert with rows
+    L.NT_max = (N + bn - 1) / bn + (choose_paired(p) ? 2 * E : E);
     L.nchunks = (N + 1023) / 1024;
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -207,6 +220,14 @@ moeffn_status moeffn_tile_n(const moeffn_problem* p, int32_t* tile_n) {
     return MOEFFN_OK;
 }
 
+moeffn_status moeffn_paired_tiles(const moeffn_problem* p, int32_t* paired) {
+    const moeffn_status s = check_problem(p);
+    if (s != MOEFFN_OK) return s;
+    if (!paired) return MOEFFN_ERR_INVALID_ARG;
+    *paired = choose_paired(*p) ? 1 : 0;
+    return MOEFFN_OK;
+}
+
 moeffn_status moeffn_workspace_bytes(const moeffn_problem* p, size_t* bytes) {
     const moeffn_status s = check_problem(p);
     if (s != MOEFFN_OK) return s;
@@ -296,7 +317,8 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
     int* slots = reinterpret_cast<int*>(w + L.slots);
 
     int* l1_done = reinterpret_cast<int*>(w + L.l1_done);
-    LayoutArgs la{x, x_sf, topk_idx, topk_w, T, H, E, k, tile_n,
+    const int paired = choose_paired(*p) ? 1 : 0;
+    LayoutArgs la{x, x_sf, topk_idx, topk_w, T, H, E, k, tile_n, paired,
                   reinterpret_cast<int*>(w + L.hist), reinterpret_cast<int*>(w + L.rank), counts, offsets,
                   tiles, tile_rows, tile_rec, l1_done, slots, reinterpret_cast<int*>(w + L.row2tk), reinterpret_cast<float*>(w + L.wpool),
                   reinterpret_cast<int*>(w + L.slack), w + L.xpool, reinterpret_cast<uint32_t*>(w + L.xpool_sf),
@@ -338,6 +360,7 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
     g.fast_math = p->fast_math;
     g.num_sms = num_sms;
     g.tile_n = tile_n;
+    g.paired = paired;
 
     g.l1_done = l1_done;
     if (p->debug_flags & MOEFFN_DEBUG_DUMP_L1_ACC) {

@@ -77,31 +77,36 @@ constexpr int pick_producers(int sr) {
 // accumulator region (the widest tile it holds).  NACC regions are used in
 // turn by the tiles of a pair (tile i -> region i % NACC), so with three or
 // more regions an MMA warp starts its next tile while the epilogue still
-// drains its previous one.
-template <int BN, int RW>
+// drains its previous one.  PAIRED: one ring whose stages hold one weight
+// tile and the halves of two token tiles of its expert (MMA warp w takes
+// token tile w of every stage); otherwise one ring per MMA warp, one token
+// tile per stage.
+template <int BN, int RW, bool PAIRED>
 struct GemmCfg {
-    static constexpr int BH = BN / 2;                   // token rows staged per CTA, at most
+    static constexpr int TPS = PAIRED ? 2 : 1;          // token tiles per stage
+    static constexpr int BH = BN / 2;                   // token rows staged per CTA and tile, at most
     static constexpr int A_BYTES = 128 * 128;           // 128 weight rows x 128 K (E2M1, 16-byte padded)
     // a TMA load of packed E2M1 (16U4_ALIGN16B) signals the packed global bytes
     // as its transaction count although it fills A_BYTES of shared memory
     static constexpr int A_TX_BYTES = A_BYTES / 2;
-    static constexpr int B_BYTES = BH * 128;
+    static constexpr int B_BYTES = BH * 128;            // a multiple of 1024 (BH: a multiple of 8)
     // operand tiles of a stage, 1024-byte aligned for the 128-byte swizzle
-    static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES + 1023) / 1024 * 1024;
+    static constexpr int STAGE_BYTES = (A_BYTES + TPS * B_BYTES + 1023) / 1024 * 1024;
     // scales of a stage, kept apart from the tiles: 512 B weight-row scales,
-    // then one 512-byte chunk of token scales per 128 tile rows
+    // then per token tile one 512-byte chunk of token scales per 128 tile rows
     static constexpr int SFB_BYTES = BN <= 128 ? 512 : 1024;
-    static constexpr int SF_STAGE = 512 + SFB_BYTES;
+    static constexpr int SF_STAGE = 512 + TPS * SFB_BYTES;
     // per gate/up warp pair two BF16 exchange buffers (L1); per pair warp a vote word
     static constexpr int XCH_BYTES = (kEpiWarps / 2) * 2 * kXchElems * 2;
     static constexpr int EPI_BYTES = XCH_BYTES + 4 * kEpiWarps;
     static constexpr int FIXED = 1024 + EPI_BYTES + 256;
     static constexpr int STAGES_FIT = (232448 - FIXED) / (STAGE_BYTES + SF_STAGE);
     static constexpr int STAGES_CAP = STAGES_FIT > 12 ? 12 : STAGES_FIT;
-    static constexpr int RING = STAGES_CAP / 2;                // stages per MMA warp
-    static constexpr int STAGES = 2 * RING;
+    static constexpr int RINGS = PAIRED ? 1 : kMmaWarps;
+    static constexpr int RING = STAGES_CAP / RINGS;            // stages per ring
+    static constexpr int STAGES = RINGS * RING;
     static constexpr int PRODUCERS = pick_producers(RING);     // producer warps per ring
-    static constexpr int THREADS = 32 * (kEpiWarps + kMmaWarps + 2 * PRODUCERS);
+    static constexpr int THREADS = 32 * (kEpiWarps + kMmaWarps + RINGS * PRODUCERS);
     static constexpr int SMEM = FIXED + STAGES * (STAGE_BYTES + SF_STAGE);
     static constexpr int SF_SET_COLS = 12;              // SFA 4 | SFB 8; per MMA warp two sets alternating by K block
     static constexpr int SF_COLS = kMmaWarps * 2 * SF_SET_COLS;
@@ -110,12 +115,15 @@ struct GemmCfg {
     static constexpr int SF_COL = NACC * RW;
     static constexpr int TMEM_NEED = NACC * RW + SF_COLS;
     static constexpr int TMEM_COLS = TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
+    // 32-column chunks of a region per epilogue warp, at most
+    static constexpr int MAXC = ((RW + 31) / 32 + kEpiGroups - 1) / kEpiGroups;
     static_assert(TMEM_NEED <= 512, "tensor memory overflow");
     static_assert(BN % 16 == 0 && BN <= kMaxTileN && RW % kTileQuantum == 0 && RW <= BN, "token tile");
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(NACC >= 2, "at least two accumulator regions");
     static_assert(RING >= 2, "pipeline too shallow");
     static_assert(RING % PRODUCERS == 0, "each producer warp owns whole stages");
+    static_assert(B_BYTES % 1024 == 0, "second token tile of a stage on a swizzle-atom boundary");
 };
 
 // token-tile TMA boxes per CTA (half a tile): 8, 16, ..., kMaxTileN / 2 rows
@@ -235,11 +243,11 @@ __device__ __forceinline__ void pair_sync(int pi) {
     }
 }
 
-template <int BN, int RW>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, RW>::THREADS, 1)
+template <int BN, int RW, bool PAIRED>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, RW, PAIRED>::THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant__ LayerMaps m2,
                     const GemmArgs p) {
-    using C = GemmCfg<BN, RW>;
+    using C = GemmCfg<BN, RW, PAIRED>;
     constexpr int S = C::STAGES, ACC = C::NACC;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -264,9 +272,10 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             // the leader's "stage full" counts the bytes of both CTAs' copies
-            // (they signal it directly); the peer's own is unused
+            // (they signal it directly); the peer's own is unused.  A paired
+            // stage is free once both MMA warps' reads of it are complete.
             mbar_init(full(s), 1);
-            mbar_init(empty(s), 1);
+            mbar_init(empty(s), PAIRED ? kMmaWarps : 1);
         }
         for (int a = 0; a < ACC; ++a) {
             mbar_init(tfull(a), 1);
@@ -311,6 +320,15 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
     // an L2 item in the same launch as the L1 items waits for its token tile's rows
     const bool wait_l1 = sc.n1 > 0;
     const int l1_target = 2 * kEpiWarps * sc.ncb1;    // one count per epilogue warp of both CTAs per L1 item
+    // Items of this pair in the order its MMA warps and its epilogue take them.
+    // Paired: items 2u and 2u + 1 (the two token tiles of one weight block,
+    // every expert having an even number of tiles) form unit u, units u = pair,
+    // pair + P, ... run in turn, MMA warp w taking item 2u + w.  Otherwise MMA
+    // warp w takes items pair + w P, pair + (w + 2) P, ...  Either way the
+    // pair's i-th item has ordinal i and accumulator region i % NACC.
+    auto item_at = [&](int i) {
+        return PAIRED ? 2 * (pair + (i >> 1) * npairs) + (i & 1) : pair + i * npairs;
+    };
 
     if (warp >= kFirstProducerWarp) {
         // ------------------------------------------------------------ TMA (both CTAs)
@@ -326,18 +344,26 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
             uint32_t armed[C::RING] = {};
             const bool starve = (p.debug_flags & 1) && rank == 0 && ring == 0;
             bool ok = true;
-            const int t_first = pair + ring * npairs;
+            // item sequence of this ring: paired, the first item of every unit
+            const int t_first = PAIRED ? item_at(0) : pair + ring * npairs;
+            const int t_step = 2 * npairs;
             TileRec rec = t_first < total ? item_rec(t_first, sc, p) : TileRec{};
-            for (int t = t_first; t < total && ok; t += 2 * npairs) {
+            for (int t = t_first; t < total && ok; t += t_step) {
                 const TileInfo ti = item_info(t, sc, rec);
                 const int layer = item_layer(t, sc);
                 const LayerMaps& m = layer == 1 ? m1 : m2;
                 const int nkb = sc.nkb(layer), a_rows = sc.rows(layer);
-                if (t + 2 * npairs < total) rec = item_rec(t + 2 * npairs, sc, p);
-                if (layer == 2 && wait_l1 &&
-                    !wait_l1_rows(p.l1_done + ti.tile_idx, l1_target, abort_flag, p.timeout_ns, p.status)) {
-                    ok = false;
-                    break;
+                if (t + t_step < total) rec = item_rec(t + t_step, sc, p);
+                if (layer == 2 && wait_l1) {
+                    bool rows_ok = wait_l1_rows(p.l1_done + ti.tile_idx, l1_target, abort_flag, p.timeout_ns,
+                                                p.status);
+                    if (PAIRED && rows_ok)
+                        rows_ok = wait_l1_rows(p.l1_done + ti.tile_idx + 1, l1_target, abort_flag, p.timeout_ns,
+                                               p.status);
+                    if (!rows_ok) {
+                        ok = false;
+                        break;
+                    }
                 }
                 const int mrow = ti.cb * 256 + 128 * static_cast<int>(rank);   // first weight row of this CTA
                 const bool mine_valid = mrow < a_rows;                          // false only for an L2 tail half
@@ -349,7 +375,10 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
                 const int box = box_for_half(half);
                 const CUtensorMap* tmBox = &m.b.m[box];
                 const int brow = ti.row0 + half * static_cast<int>(rank);
-                const uint32_t bytes = C::A_TX_BYTES + box_half_rows(box) * 128 + 512 + C::SFB_BYTES;
+                // paired: the unit's second tile is the next tile of the expert
+                // (rows ti.ncols further on, scale rows nkb further on)
+                const uint32_t bytes =
+                    C::A_TX_BYTES + C::TPS * (box_half_rows(box) * 128 + C::SFB_BYTES) + 512;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (ls % C::PRODUCERS != pw) {
                         if (++ls == C::RING) {
@@ -366,13 +395,17 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
                     }
                     const uint32_t sb = sbase + stage * C::STAGE_BYTES;
                     const uint32_t ss = sfbase + stage * C::SF_STAGE;
-                    if (!(starve && t == pair && layer == 1 && kb == 0)) {
+                    if (!(starve && t == t_first && layer == 1 && kb == 0)) {
                         const uint32_t fb = leader_full0 + 8u * stage;
                         if (rank == 0) mbar_arrive_expect_tx_w(full(stage), 2 * bytes);
                         tma_load_2d_pair_w(sb, &m.a, fb, kb * 128, a0);
                         tma_load_2d_pair_w(sb + C::A_BYTES, tmBox, fb, kb * 128, brow);
                         tma_load_2d_pair_w(ss, &m.sfa, fb, 0, sfa_row + kb);
                         tma_load_2d_pair_w(ss + 512, &m.sfb, fb, 0, sfb_row + kb);
+                        if (PAIRED) {
+                            tma_load_2d_pair_w(sb + C::A_BYTES + C::B_BYTES, tmBox, fb, kb * 128, brow + ti.ncols);
+                            tma_load_2d_pair_w(ss + 512 + C::SFB_BYTES, &m.sfb, fb, 0, sfb_row + nkb + kb);
+                        }
                         ++armed[ls];
                     }
                     if (++ls == C::RING) {
@@ -396,7 +429,7 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
         }
         __syncwarp();
     } else if (warp >= kFirstMmaWarp) {
-        const int ring = warp - kFirstMmaWarp;               // tiles of this parity, accumulator `ring`
+        const int mw = warp - kFirstMmaWarp;                 // this warp's items (see item_at)
         if (rank == 0) {
             // ---------------------------------------------------- MMA (leader)
             // the whole warp runs the loop; one elected lane issues each instruction
@@ -404,8 +437,12 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
             int ls = 0, it = 0;
             uint32_t phase = 0, kiter = 0;
             bool ok = true;
-            const uint32_t sf_base = tmem + C::SF_COL + static_cast<uint32_t>(ring * 2 * C::SF_SET_COLS);
-            const int t_first = pair + ring * npairs;
+            const uint32_t sf_base = tmem + C::SF_COL + static_cast<uint32_t>(mw * 2 * C::SF_SET_COLS);
+            // paired: this warp's token tile of every stage of the one ring
+            const int ring = PAIRED ? 0 : mw;
+            const uint32_t b_off = C::A_BYTES + (PAIRED ? mw * C::B_BYTES : 0);
+            const uint32_t sfb_off = 512 + (PAIRED ? mw * C::SFB_BYTES : 0);
+            const int t_first = PAIRED ? 2 * pair + mw : pair + mw * npairs;
             TileRec rec = t_first < total ? item_rec(t_first, sc, p) : TileRec{};
             for (int t = t_first; t < total && ok; t += 2 * npairs, ++it) {
                 const TileInfo ti = item_info(t, sc, rec);
@@ -413,7 +450,7 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
                 if (t + 2 * npairs < total) rec = item_rec(t + 2 * npairs, sc, p);
                 const uint32_t idesc_n = IDESC | (static_cast<uint32_t>(ti.ncols >> 3) << 17);
                 const bool two_sfb = ti.ncols > 128;
-                const int tord = 2 * it + ring;                // ordinal of this tile in the pair's sequence
+                const int tord = 2 * it + mw;                  // ordinal of this tile in the pair's sequence
                 const int as = tord % ACC;
                 const uint32_t ap = static_cast<uint32_t>(tord / ACC) & 1u;
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded<true>(tempty(as), ap ^ 1u, abort_flag, p.timeout_ns,
@@ -438,10 +475,10 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
                     const uint32_t sfs = sf_base + (kiter & 1u) * C::SF_SET_COLS;
                     ++kiter;
                     // descriptors of the stage; a K step of 32 bytes adds 2 to the address field
-                    const uint64_t adesc = desc_kmajor_sw128(sb), bdesc = desc_kmajor_sw128(sb + C::A_BYTES);
+                    const uint64_t adesc = desc_kmajor_sw128(sb), bdesc = desc_kmajor_sw128(sb + b_off);
                     tc_cp_sf_pair_w(sfs, desc_sf_block(ss));
-                    tc_cp_sf_pair_w(sfs + 4, desc_sf_block(ss + 512));
-                    if (two_sfb) tc_cp_sf_pair_w(sfs + 8, desc_sf_block(ss + 1024));
+                    tc_cp_sf_pair_w(sfs + 4, desc_sf_block(ss + sfb_off));
+                    if (two_sfb) tc_cp_sf_pair_w(sfs + 8, desc_sf_block(ss + sfb_off + 512));
                     tc_mma_mx_pair_w(d, adesc, bdesc, idk[0], sfs, sfs + 4, kb != 0);
                     tc_mma_mx_pair_w(d, adesc + 2, bdesc + 2, idk[1], sfs, sfs + 4, 1u);
                     tc_mma_mx_pair_w(d, adesc + 4, bdesc + 4, idk[2], sfs, sfs + 4, 1u);
@@ -466,12 +503,13 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
         const int grp = warp >> 2;                           // this warp takes chunks grp, grp + 3, ...
         const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
         const uint32_t leader_tempty0 = map_shared_rank(tempty(0), 0);
-        int it = 0;
-        TileRec rec = pair < total ? item_rec(pair, sc, p) : TileRec{};
-        for (int t = pair; t < total; t += npairs, ++it) {
+        TileRec rec = item_at(0) < total ? item_rec(item_at(0), sc, p) : TileRec{};
+        for (int it = 0;; ++it) {
+            const int t = item_at(it);
+            if (t >= total) break;
             const TileInfo ti = item_info(t, sc, rec);
             const bool l1 = item_layer(t, sc) == 1;
-            if (t + npairs < total) rec = item_rec(t + npairs, sc, p);
+            if (item_at(it + 1) < total) rec = item_rec(item_at(it + 1), sc, p);
             const int as = it % ACC;
             const uint32_t ap = static_cast<uint32_t>(it / ACC) & 1u;
             const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(tfull(as), ap, abort_flag, p.timeout_ns,
@@ -492,44 +530,65 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
             const uint32_t tacc = tq + static_cast<uint32_t>(as * RW);
             const int nchunks = (ti.nvalid + 31) / 32;
             const int mrow = ti.cb * 256 + 128 * static_cast<int>(rank);
-            if (l1) {
-                // Quarter q holds band q of this CTA's 128 rows: gate (q even) or up
-                // (q odd) of channels cbase + [0, 32), cbase = mrow / 2 + 32 (q / 2);
-                // thread `lane` has channel cbase + lane for the chunk's 32 tokens.
-                // The gate warp finishes tokens 0-15 of a chunk and the up warp tokens
-                // 16-31; each hands the other the half of its values that it needs.
-                const int pr = q >> 1, hs = q & 1, pi = warp >> 1;
-                __nv_bfloat16* XG = xch + (2 * pi) * kXchElems;     // gate of tokens 16-31, for the up warp
-                __nv_bfloat16* XU = XG + kXchElems;                 // up of tokens 0-15, for the gate warp
-                const int cbase = mrow / 2 + 32 * pr;
-                const int mine0 = 16 * hs;                          // first token of this warp's half
-                const float clamp = p.act_clamp;
-                for (int j = grp; j < nchunks; j += kEpiGroups) {
-                    float v[32];
-                    tmem_ld32(tacc + 32 * j, v);
-                    if (p.debug_flags & 2) {
+            // L1: quarter q holds band q of this CTA's 128 rows: gate (q even) or
+            // up (q odd) of channels cbase1 + [0, 32), cbase1 = mrow / 2 + 32 (q / 2);
+            // thread `lane` has channel cbase1 + lane for the chunk's 32 tokens
+            const int hs = q & 1;
+            const int cbase1 = mrow / 2 + 32 * (q >> 1);
+            // This warp's chunks (grp + 3 c) of the region, as BF16 pairs: pk[c][i]
+            // holds tokens 2 i and 2 i + 1.  Both epilogues round the accumulators to
+            // BF16 first, so the region is released before any arithmetic on them.
+            uint32_t pk[C::MAXC][16];
+#pragma unroll
+            for (int c = 0; c < C::MAXC; ++c) {
+                const int j = grp + kEpiGroups * c;
+                if (j < nchunks) {
+                    uint32_t r[32];
+                    tmem_ld32_issue(tacc + 32 * j, r);
+                    tmem_ld_wait(r);
+                    if (l1 && (p.debug_flags & 2)) {
                         // test hook: raw FP32 accumulators, [P_max][gate I | up I] floats
-                        // (unrolled: a runtime index into v would move v to local memory)
                         float* zd = reinterpret_cast<float*>(p.ypool);
 #pragma unroll
                         for (int n = 0; n < 32; ++n)
                             if (32 * j + n < ti.nvalid)
-                                zd[static_cast<size_t>(ti.row0 + 32 * j + n) * 2 * p.I + hs * p.I + cbase + lane] = v[n];
+                                zd[static_cast<size_t>(ti.row0 + 32 * j + n) * 2 * p.I + hs * p.I + cbase1 + lane] =
+                                    __uint_as_float(r[n]);
                     }
-                    // this warp's half and the half it hands over, selected with constant
-                    // indices so that v stays in registers
-                    float mine[16], other[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        mine[i] = hs ? v[16 + i] : v[i];
-                        other[i] = hs ? v[i] : v[16 + i];
+                    for (int i = 0; i < 16; ++i) pk[c][i] = bf16x2_bits(r[2 * i], r[2 * i + 1]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            // relaxed: what the MMA warp must not overtake are this warp's TMEM loads,
+            // complete (tcgen05.wait::ld) and fenced above; the rows stored to global
+            // memory are not read by that warp, and a release would wait for them
+            if (lane == 0) mbar_arrive_remote_relaxed(leader_tempty0 + 8u * as);
+            if (l1) {
+                // The gate warp finishes tokens 0-15 of a chunk and the up warp tokens
+                // 16-31; each hands the other the half of its values that it needs.
+                const int pi = warp >> 1;
+                __nv_bfloat16* XG = xch + (2 * pi) * kXchElems;     // gate of tokens 16-31, for the up warp
+                __nv_bfloat16* XU = XG + kXchElems;                 // up of tokens 0-15, for the gate warp
+                const int cbase = cbase1;
+                const int mine0 = 16 * hs;                          // first token of this warp's half
+                const float clamp = p.act_clamp;
+#pragma unroll
+                for (int c = 0; c < C::MAXC; ++c) {
+                    const int j = grp + kEpiGroups * c;
+                    if (j >= nchunks) break;                        // the same for both warps of the pair
+                    // this warp's half and the half it hands over (constant indices, so
+                    // that pk stays in registers)
+                    uint32_t mw2[8], ow2[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        mw2[i] = hs ? pk[c][8 + i] : pk[c][i];
+                        ow2[i] = hs ? pk[c][i] : pk[c][8 + i];
                     }
-                    // g and u enter SwiGLU rounded to BF16, so the hand-over holds BF16
                     __nv_bfloat16* give = hs ? XU : XG;
 #pragma unroll
-                    for (int i = 0; i < 16; i += 2)
-                        *reinterpret_cast<__nv_bfloat162*>(give + lane * kXchLd + i) =
-                            __floats2bfloat162_rn(other[i], other[i + 1]);
+                    for (int i = 0; i < 8; ++i) *reinterpret_cast<uint32_t*>(give + lane * kXchLd + 2 * i) = ow2[i];
                     // top-k weights of this half's 16 tokens, one per lane, broadcast below
                     const int r16 = 32 * j + mine0 + (lane & 15);
                     const float wl = r16 < ti.nvalid ? __ldg(p.wpool + ti.row0 + r16) : 0.f;
@@ -540,7 +599,7 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
                     for (int i = 0; i < 16; i += 2) {
                         const float2 o = __bfloat1622float2(
                             *reinterpret_cast<const __nv_bfloat162*>(take + lane * kXchLd + i));
-                        const float m0 = bf16_round(mine[i]), m1 = bf16_round(mine[i + 1]);
+                        const float m0 = bf16_lo(mw2[i / 2]), m1 = bf16_hi(mw2[i / 2]);
                         g[i] = hs ? o.x : m0;
                         u[i] = hs ? m0 : o.x;
                         g[i + 1] = hs ? o.y : m1;
@@ -615,39 +674,36 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
                     pair_sync(pi);                                  // the buffers are free for the next chunk
                 }
             } else if (mrow < p.H) {
-                // thread `lane` has output channel cbase + lane for the chunk's 32 tokens;
-                // 16 tokens at a time are staged as BF16 [token][32 channels] (in this
-                // warp's share of the exchange buffers, unused by this layer) so that
-                // each lane stores 32 contiguous bytes of a row
-                const int cbase = mrow + 32 * q;
-                // lanes 2m and 2m + 1 swap halves: the even lane then holds channels
+                // thread `lane` has output channel cbase + lane for the chunk's 32 tokens.
+                // Lanes 2m and 2m + 1 swap halves: the even lane then holds channels
                 // (2m, 2m + 1) of tokens 0-15, the odd lane of tokens 16-31, and each
                 // stores one BF16 pair per token (the warp writes 64 contiguous bytes)
+                const int cbase = mrow + 32 * q;
                 const bool odd = lane & 1;
                 const int c2 = cbase + (lane & ~1);
-                for (int j = grp; j < nchunks; j += kEpiGroups) {
-                    float v[32];
-                    tmem_ld32(tacc + 32 * j, v);
-                    const int nrows = min(32, ti.nvalid - 32 * j);
+#pragma unroll
+                for (int c = 0; c < C::MAXC; ++c) {
+                    const int j = grp + kEpiGroups * c;
+                    if (j >= nchunks) break;
+                    const int nrows = min(32, ti.nvalid - 32 * j) - (odd ? 16 : 0);
                     uint16_t* dst = p.ypool + static_cast<size_t>(ti.row0 + 32 * j + (odd ? 16 : 0)) * p.H + c2;
 #pragma unroll
-                    for (int n = 0; n < 16; ++n) {
-                        // even lane sends its token 16 + n, odd lane its token n
-                        const float send = odd ? v[n] : v[16 + n];
-                        const float got = __shfl_xor_sync(0xffffffffu, send, 1);
-                        const float keep = odd ? v[16 + n] : v[n];
-                        const __nv_bfloat162 b2 = odd ? __floats2bfloat162_rn(got, keep) : __floats2bfloat162_rn(keep, got);
-                        if (n + (odd ? 16 : 0) < nrows)
-                            *reinterpret_cast<__nv_bfloat162*>(dst + static_cast<size_t>(n) * p.H) = b2;
+                    for (int i = 0; i < 8; ++i) {
+                        // tokens 2i, 2i + 1 of this lane's half: the even lane sends its
+                        // tokens 16 + 2i, 16 + 2i + 1, the odd lane its tokens 2i, 2i + 1
+                        const uint32_t send = odd ? pk[c][i] : pk[c][8 + i];
+                        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                        const uint32_t keep = odd ? pk[c][8 + i] : pk[c][i];
+                        const uint32_t ch0 = odd ? recv : keep, ch1 = odd ? keep : recv;   // channels c2, c2 + 1
+                        if (2 * i < nrows)
+                            *reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(2 * i) * p.H) =
+                                __byte_perm(ch0, ch1, 0x5410);
+                        if (2 * i + 1 < nrows)
+                            *reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(2 * i + 1) * p.H) =
+                                __byte_perm(ch0, ch1, 0x7632);
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            // relaxed: what the MMA warp must not overtake are this warp's TMEM loads,
-            // complete (tcgen05.wait::ld) and fenced above; the rows stored to global
-            // memory are not read by that warp, and a release would wait for them
-            if (lane == 0) mbar_arrive_remote_relaxed(leader_tempty0 + 8u * as);
             if (l1 && wait_l1) {
                 // publish this warp's share of the token tile's L1 rows and scales to
                 // the L2 items of the same launch, which read them by TMA (the
@@ -669,10 +725,10 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
     }
 }
 
-template <int BN, int RW>
+template <int BN, int RW, bool PAIRED>
 static cudaError_t launch_one(const GemmMaps& g1, const GemmMaps& g2, const GemmArgs& a, cudaStream_t stream) {
-    using C = GemmCfg<BN, RW>;
-    auto kernel = grouped_gemm_kernel<BN, RW>;
+    using C = GemmCfg<BN, RW, PAIRED>;
+    auto kernel = grouped_gemm_kernel<BN, RW, PAIRED>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (err != cudaSuccess) return err;
     // persistent grid: as many CTA pairs as can be resident at once (an L2 item
@@ -708,12 +764,17 @@ static cudaError_t launch_one(const GemmMaps& g1, const GemmMaps& g2, const Gemm
 }
 
 cudaError_t launch_gemm(const GemmMaps& m1, const GemmMaps& m2, const GemmArgs& a, cudaStream_t stream) {
-    // three stage layouts: tiles of at most 32 rows (10 stages in flight, four
-    // accumulator regions), at most 144 rows (8 stages, three regions) and at
-    // most kMaxTileN rows (6 stages, two regions)
-    if (a.tile_n <= 32) return launch_one<32, 32>(m1, m2, a, stream);
-    if (a.tile_n <= 144) return launch_one<144, 144>(m1, m2, a, stream);
-    return launch_one<kMaxTileN, kMaxTileN>(m1, m2, a, stream);
+    // stage layouts: tiles of at most 32 rows (10 stages in flight, four
+    // accumulator regions); tiles of at most 144 rows, one per stage (8 stages,
+    // three regions) or paired (5 stages of one weight tile and two token
+    // tiles, three regions); tiles of at most kMaxTileN rows (6 stages, two
+    // regions)
+    static_assert(!pairable_tile_n(32) && pairable_tile_n(48) && pairable_tile_n(144) && !pairable_tile_n(160),
+                  "the paired layout is the 144-row one");
+    if (a.tile_n <= 32) return launch_one<32, 32, false>(m1, m2, a, stream);
+    if (a.tile_n <= 144)
+        return a.paired ? launch_one<144, 144, true>(m1, m2, a, stream) : launch_one<144, 144, false>(m1, m2, a, stream);
+    return launch_one<kMaxTileN, kMaxTileN, false>(m1, m2, a, stream);
 }
 
 }  // namespace moeffn

@@ -9,12 +9,20 @@ namespace moeffn {
 
 struct DevStatus;
 
+// Tile bounds from 48 to 144 rows use the 144-row stage layout, which has a
+// paired form: every expert's rows are split into an even number of equal
+// token tiles, and the two tiles of a pair share each weight stage of the
+// grouped GEMM (two MMA warps, one per tile, consume every stage).  The host
+// pairs when an expert is expected to have more than one tile.
+constexpr bool pairable_tile_n(int tile_n) { return tile_n > 32 && tile_n <= 144; }
+
 struct LayoutArgs {
     const uint8_t* x;
     const uint32_t* x_sf;
     const int64_t* topk_idx;
     const float* topk_w;
     int T, H, E, k, tile_n;   // tile_n: most token rows per GEMM tile
+    int paired;               // an even number of tiles per expert (pairable_tile_n(tile_n) only)
     int* hist;      // [ceil(T*k/1024)][E]
     int* rank;      // [T*k]
     int* counts;    // [E]
@@ -63,6 +71,7 @@ struct GemmArgs {
     int fast_math;          // 1: SiLU with approximate exp and reciprocal
     int num_sms;
     int tile_n;             // most token rows per tile (selects the stage layout)
+    int paired;             // pairs of token tiles per stage (LayoutArgs::paired)
     int run_l1, run_l2;     // which layers' items this launch runs (L1 items first)
     int* l1_done;           // [NT_max] per token tile: L1 epilogue warps that published their rows
 };

@@ -133,7 +133,7 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int
 }
 
 __global__ void __launch_bounds__(kChunk) layout_count_kernel(
-    const int64_t* __restrict__ topk_idx, int N, int E, int tile_n, int* __restrict__ hist,
+    const int64_t* __restrict__ topk_idx, int N, int E, int tile_n, int paired, int* __restrict__ hist,
     int* __restrict__ rank, int* __restrict__ counts, int* __restrict__ offsets,
     int* __restrict__ tiles, int* __restrict__ tile_rows, DevStatus* st) {
     extern __shared__ int s_wcnt[];   // [32 warps][E]
@@ -196,8 +196,10 @@ __global__ void __launch_bounds__(kChunk) layout_count_kernel(
     const int off = block_exclusive_scan_1024(padded, s_warp, total);
     if (tid < E) offsets[tid] = off;
     if (tid == 0) offsets[E] = total;
-    // tiles of an expert: as few as tile_n allows, equal, a multiple of 16 rows
-    const int ntile = tid < E ? (cnt + tile_n - 1) / tile_n : 0;
+    // tiles of an expert: as few as tile_n allows (an even number when paired),
+    // equal, a multiple of 16 rows
+    int ntile = tid < E ? (cnt + tile_n - 1) / tile_n : 0;
+    if (paired) ntile += ntile & 1;
     const int toff = block_exclusive_scan_1024(ntile, s_warp, total);
     if (tid < E) {
         tiles[tid] = toff;
@@ -321,7 +323,7 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
         if (err != cudaSuccess) return err;
     }
     cudaError_t err = launch_pdl(layout_count_kernel, dim3(nchunks), dim3(kChunk), smem, stream, a.topk_idx, N,
-                                 a.E, a.tile_n, a.hist, a.rank, a.counts, a.offsets, a.tiles, a.tile_rows,
+                                 a.E, a.tile_n, a.paired, a.hist, a.rank, a.counts, a.offsets, a.tiles, a.tile_rows,
                                  a.status);
     if (err != cudaSuccess) return err;
     const int tok_per_block = 8 / kDispatchSplit;

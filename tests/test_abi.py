@@ -76,6 +76,19 @@ def test_tile_n_choice():
     assert mb.tile_n(mb.problem(128, 1024, 512, 8, 2, tile_n=128)) == 128
 
 
+def test_paired_tiles_choice():
+    # pairs of token tiles per weight stage when an expert expects more than one
+    # tile (T*k > tile_n*E) and the tile bound is 48..144
+    assert mb.paired_tiles(mb.problem(8192, 7168, 2048, 256, 8))           # prefill: 256 > 144 rows
+    assert mb.paired_tiles(mb.problem(2048, 4096, 1536, 64, 8))            # 256 rows per expert
+    assert not mb.paired_tiles(mb.problem(4000, 7168, 2048, 256, 8))       # 125 rows per expert
+    assert not mb.paired_tiles(mb.problem(128, 7168, 2048, 256, 8))        # decode: 32-row tiles
+    assert not mb.paired_tiles(mb.problem(8192, 7168, 2048, 64, 8))        # 224-row tiles
+    assert mb.paired_tiles(mb.problem(200, 256, 128, 5, 2, tile_n=48))     # 80 > 48 rows
+    assert not mb.paired_tiles(mb.problem(200, 256, 128, 5, 2, tile_n=96))
+    assert not mb.paired_tiles(mb.problem(200, 256, 128, 5, 2, tile_n=160))
+
+
 @pytest.mark.parametrize("T,H,I,E,k", [(128, 1024, 512, 8, 2), (8192, 7168, 2048, 256, 8),
                                        (4000, 7168, 2048, 256, 8), (0, 256, 128, 4, 1)])
 def test_buffer_sizes(T, H, I, E, k):

@@ -84,15 +84,21 @@ def test_checked_rows_cover_every_token_tile(name):
     checked = np.zeros(tabs["P"], bool)
     checked[slots[slots >= 0]] = True
     off, counts, tiles, per = tabs["offsets"], tabs["counts"], tabs["tiles"], tabs["tile_rows"]
-    n_tiles = 0
+    n_tiles = n_empty = 0
     for e in range(wl.E):
         for t in range(int(tiles[e + 1] - tiles[e])):
             lo = int(off[e]) + t * int(per[e])
             hi = int(off[e]) + min(int(counts[e]), (t + 1) * int(per[e]))
+            if hi <= lo:
+                # the second tile of an expert with at most 16 rows (an even
+                # number of tiles): it owns no rows, and no output comes from it
+                assert mb.paired_tiles(run.prob) and t == 1 and counts[e] <= 16, (e, t)
+                n_empty += 1
+                continue
             assert checked[lo] and checked[hi - 1], (e, t)
             n_tiles += 1
     print(f"{name}: {int(checked.sum())} of {int(counts.sum())} pool rows checked, "
-          f"{len(tokens)} of {wl.T} tokens, {n_tiles} token tiles")
+          f"{len(tokens)} of {wl.T} tokens, {n_tiles} token tiles (+ {n_empty} without rows)")
 
 
 @pytest.mark.parametrize("name", CONFIGS)
@@ -138,6 +144,8 @@ def test_layout_parity(name):
         assert np.array_equal(got[key], ref[key]), key
     assert got["P"] == ref["P"]
     ntile = -(-ref["counts"] // run.tile_n)
+    if mb.paired_tiles(run.prob):
+        ntile += ntile & 1                            # an even number of tiles per expert
     assert np.array_equal(got["tiles"], np.concatenate([[0], np.cumsum(ntile)]))
     # equal tiles, rounded up to the 16-row quantum of the tile layout
     per = np.where(ntile > 0, -(-ref["counts"] // np.maximum(ntile, 1)), 16)
@@ -225,11 +233,15 @@ def _check_full(inp, idx, w, run, clamp=0.0):
     assert max_rel <= Y_MAX_REL and mean_rel <= Y_MEAN_REL, (max_rel, mean_rel)
 
 
-@pytest.mark.parametrize("tile_n", [32, 48, 64, 96, 128, 144, 160, 192, 224])
-def test_every_token_tile(tile_n):
-    inp, idx, w = _small(T=200, E=5, k=2, skew=True)
+@pytest.mark.parametrize("tile_n,T", [(32, 200), (48, 200), (64, 200), (96, 200), (128, 200), (144, 200),
+                                      (160, 200), (192, 200), (224, 200), (96, 700), (144, 700)])
+def test_every_token_tile(tile_n, T):
+    # T = 200 pairs tiles at bounds 48 and 64 (80 rows per expert expected),
+    # T = 700 at 96 and 144 as well (280 rows)
+    inp, idx, w = _small(T=T, E=5, k=2, skew=True)
     run = GpuRun(inp, idx, w, tile_n=tile_n)
     assert run.tile_n == tile_n and run.status()[0] == mb.OK
+    assert mb.paired_tiles(run.prob) == (tile_n in (48, 64) or (T == 700 and tile_n in (96, 144)))
     _check_full(inp, idx, w, run)
 
 
@@ -326,9 +338,12 @@ def test_l1_accumulators_match_exact_products():
     """Raw FP32 accumulators of the block-scaled tensor-core GEMM against the
     fp64 sum of exactly representable products."""
     from oracle.grouped import _dequant_act, _dequant_w
-    inp, idx, w = _small(T=70, H=1024, I=256, E=3, k=2, seed=5)
-    for tile_n in (32, 96, 144, 224):
+    # (tile bound, tokens): 70 tokens give one tile per stage at every bound;
+    # 48-row tiles with 120 tokens (80 rows per expert) are paired
+    for tile_n, T in ((32, 70), (96, 70), (144, 70), (224, 70), (48, 120)):
+        inp, idx, w = _small(T=T, H=1024, I=256, E=3, k=2, seed=5)
         run = GpuRun(inp, idx, w, tile_n=tile_n, debug_flags=mb.DEBUG_DUMP_L1_ACC)
+        assert mb.paired_tiles(run.prob) == (tile_n == 48)
         tabs = run.tables()
         z = run.view("ypool", torch.float32)[: tabs["P"] * 2 * run.I].view(tabs["P"], 2 * run.I).cpu().numpy()
         assert run.status()[0] == mb.OK
@@ -346,9 +361,12 @@ def test_l1_accumulators_match_exact_products():
             assert np.all(err <= 1e-5 * mag + 1e-30), (e, tile_n, float((err / (mag + 1e-30)).max()))
 
 
-def test_bounded_wait_reports_timeout_and_context_survives():
-    inp, idx, w = _small(T=64, E=4, k=2)
-    run = GpuRun(inp, idx, w, debug_flags=mb.DEBUG_STARVE_L1, wait_timeout_us=20000)
+@pytest.mark.parametrize("tile_n,T", [(0, 64), (48, 200)])
+def test_bounded_wait_reports_timeout_and_context_survives(tile_n, T):
+    # (0, 64): 32-row tiles, one ring per MMA warp; (48, 200): paired tiles, one ring
+    inp, idx, w = _small(T=T, E=4, k=2)
+    run = GpuRun(inp, idx, w, tile_n=tile_n, debug_flags=mb.DEBUG_STARVE_L1, wait_timeout_us=20000)
+    assert mb.paired_tiles(run.prob) == (tile_n == 48)
     st, code, detail = run.status()
     # any pipeline wait may be the first of the grid to expire (a race), but it is one of them
     assert st == mb.ERR_TIMEOUT and code & 2 and 1 <= detail <= 7
