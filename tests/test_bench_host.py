@@ -48,12 +48,31 @@ def test_medium_step_model_matches_the_table():
     assert a["bytes"] == pytest.approx(8.97e8, rel=2e-3)
 
 
+def test_roofline_peaks():
+    pk = dict(hbm_gbs=6000.0, fp8_tflops=4000.0, fp8_tflops_sustained=3000.0, source="test")
+    # prefill: tensor-bound, against the sustained FP8-rate peak, burst fraction beside it
+    wl = synth.WORKLOADS["prefill"]
+    a = bench.algorithmic(wl, np.full(wl.E, wl.N // wl.E))
+    r = bench.gemm_roofline(a, 2.0, pk)
+    tf = (a["l1_flops"] + a["l2_flops"]) / 2e-3 / 1e12
+    assert r["bound"] == "tensor" and r["peak"] == 3000.0
+    assert r["frac"] == pytest.approx(tf / 3000.0) and r["frac_of_burst_peak"] == pytest.approx(tf / 4000.0)
+    assert bench.step_roofline_time(a, pk) == pytest.approx(a["flops"] / 4e15)
+    assert bench.step_roofline_time(a, pk, True) == pytest.approx(a["flops"] / 3e15)
+    # decode: weight streaming, against the HBM copy bandwidth
+    wl = synth.WORKLOADS["decode"]
+    a = bench.algorithmic(wl, np.ones(wl.E, dtype=np.int64))
+    r = bench.gemm_roofline(a, 1.0, pk)
+    assert r["bound"] == "hbm" and r["peak"] == 6000.0 and "frac_of_burst_peak" not in r
+    assert r["frac"] == pytest.approx((a["l1_bytes"] + a["l2_bytes"]) / 1e-3 / 1e9 / 6000.0)
+
+
 def test_traffic_lookup_follows_the_kernel_hash():
     text = open(os.path.join(ROOT, "profiles", "grouped_gemm_traffic.md")).read()
     recorded = text.split("kernel source sha256:")[1].split()[0]
-    assert bench.traffic_from_profile(recorded, "prefill", 1.0) == 7563061248.0
-    assert bench.traffic_from_profile(recorded, "prefill", 2.0) == 2 * 7563061248.0
-    assert bench.traffic_from_profile(recorded, "decode", 1.0) == 6009995694.0
+    assert bench.traffic_from_profile(recorded, "prefill", 1.0) == 7552239616.0
+    assert bench.traffic_from_profile(recorded, "prefill", 2.0) == 2 * 7552239616.0
+    assert bench.traffic_from_profile(recorded, "decode", 1.0) == 6010521886.0
     assert bench.traffic_from_profile("0" * 64, "prefill", 1.0) is None     # another kernel source
     assert bench.traffic_from_profile(recorded, "no-such-workload", 1.0) is None
 
