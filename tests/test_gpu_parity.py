@@ -13,9 +13,9 @@ plus 40-96 random tokens, the 8 rows with the largest activation scales
 and the last token.  Every token tile of the run has checked rows; the
 test asserts it and reports rows checked / pool rows.  With the default
 144-row tile bound that is, for medium, 128 tiles, ~340 of 2048 tokens,
-~2.7k of 16384 routed rows; prefill 515 tiles, ~1.1k of 8192 tokens,
-~8.8k of 65536 rows; skewed 381 tiles, ~930 of 4000 tokens, ~7.4k of
-32000 rows.
+~2.7k of 16384 routed rows; prefill 518 tiles (paired: an even number per
+expert), ~1.1k of 8192 tokens, ~8.9k of 65536 rows; skewed 381 tiles,
+~930 of 4000 tokens, ~7.4k of 32000 rows.
 """
 import numpy as np
 import pytest
