@@ -181,12 +181,19 @@ __global__ void __launch_bounds__(kChunk) layout_count_kernel(
     const int nchunks = gridDim.x;
     int cnt = 0;
     if (tid < E) {
+        // chunk c's first rank inside expert tid; eight chunk counts in flight at a time
         int run = 0;
-        for (int c = 0; c < nchunks; ++c) {
-            int* p = hist + static_cast<size_t>(c) * E + tid;
-            const int h = __ldcg(p);
-            *p = run;              // chunk c's first rank inside expert tid
-            run += h;
+        for (int c0 = 0; c0 < nchunks; c0 += 8) {
+            int h[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                h[u] = c0 + u < nchunks ? __ldcg(hist + static_cast<size_t>(c0 + u) * E + tid) : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c0 + u < nchunks) {
+                    hist[static_cast<size_t>(c0 + u) * E + tid] = run;
+                    run += h[u];
+                }
         }
         cnt = run;
         counts[tid] = cnt;
