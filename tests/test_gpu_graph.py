@@ -33,11 +33,14 @@ def _check_oracle(inp, k, prob, ws, idx, y):
     assert max_rel <= 2e-2 and mean_rel <= 5e-3, (max_rel, mean_rel)
 
 
-def test_forward_replays_in_a_cuda_graph():
-    wl = synth.Workload("graph", 96, 512, 256, 6, 2, 51)
+@pytest.mark.parametrize("T", [96, 600])
+def test_forward_replays_in_a_cuda_graph(T):
+    # T = 96: 32-row tiles; T = 600: paired 144-row tiles (200 rows per expert expected)
+    wl = synth.Workload("graph", T, 512, 256, 6, 2, 51)
     inp = synth.make_inputs(wl)
-    inp2 = synth.make_inputs(synth.Workload("graph2", 96, 512, 256, 6, 2, 52))
+    inp2 = synth.make_inputs(synth.Workload("graph2", T, 512, 256, 6, 2, 52))
     prob = mb.problem(wl.T, wl.H, wl.I, wl.E, wl.k)
+    assert mb.paired_tiles(prob) == (T == 600)
     prepared = mb.prepare_weights(prob, _up(inp["w1"]), _up(inp["w1_sf"]), _up(inp["w2"]), _up(inp["w2_sf"]))
     logits, x, x_sf = _up(inp["logits"]), _up(inp["x"]), _up(inp["x_sf"])
 

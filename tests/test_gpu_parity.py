@@ -266,15 +266,21 @@ def test_fast_math_meets_the_same_bars():
     _check_full(inp, idx, w, run)
 
 
-def test_empty_entries_and_ragged_tokens():
-    inp, idx, w = _small(T=37, E=7, k=3, empty=0.3)
-    run = GpuRun(inp, idx, w)
+@pytest.mark.parametrize("T,tile_n", [(37, 0), (200, 48)])
+def test_empty_entries_and_ragged_tokens(T, tile_n):
+    # (200, 48): paired 48-row tiles (~86 rows per expert expected)
+    inp, idx, w = _small(T=T, E=7, k=3, empty=0.3)
+    run = GpuRun(inp, idx, w, tile_n=tile_n)
+    assert mb.paired_tiles(run.prob) == (tile_n == 48)
     _check_full(inp, idx, w, run)
 
 
-def test_single_expert_top1():
-    inp, idx, w = _small(T=50, E=1, k=1)
+@pytest.mark.parametrize("T", [50, 200])
+def test_single_expert_top1(T):
+    # T = 200: one expert with 200 rows, paired into two 112-row tiles
+    inp, idx, w = _small(T=T, E=1, k=1)
     run = GpuRun(inp, idx, w)
+    assert mb.paired_tiles(run.prob) == (T == 200)
     _check_full(inp, idx, w, run)
 
 
@@ -284,10 +290,14 @@ def test_all_experts_per_token():
     _check_full(inp, idx, w, run)
 
 
-def test_hidden_not_multiple_of_256():
-    """L2 output channel tiles of 256 with a 128-wide remainder."""
-    inp, idx, w = _small(T=64, H=384, I=128, E=3, k=2)
+@pytest.mark.parametrize("T", [64, 300])
+def test_hidden_not_multiple_of_256(T):
+    """L2 output channel tiles of 256 with a 128-wide remainder; I = 128, so
+    an L2 item has one K block.  T = 300 pairs the token tiles (200 rows per
+    expert expected against 144-row tiles)."""
+    inp, idx, w = _small(T=T, H=384, I=128, E=3, k=2)
     run = GpuRun(inp, idx, w)
+    assert mb.paired_tiles(run.prob) == (T == 300)
     _check_full(inp, idx, w, run)
 
 
