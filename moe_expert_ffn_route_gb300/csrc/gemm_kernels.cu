@@ -32,6 +32,14 @@
 //    of at most 144 rows) fed by its own TMA warp; twelve warps drain TMEM.
 //    Items use accumulator regions in turn (three of 144 columns, two of
 //    224 or four of 32), so an MMA warp rarely waits for the epilogue.
+//  - Paired tiles (when experts expect more than one tile): every expert has
+//    an even number of tiles, and the two tiles of one weight block share
+//    each weight stage of a single ring: per K block the stage holds the
+//    weight tile once and both token halves, and MMA warp w issues tile w's
+//    MMAs.  The weights then cross L2 and shared memory once per two tiles.
+//  - The epilogue loads a finished region's chunks as BF16 pairs (both
+//    layers round the accumulators to BF16 first) and frees the region before
+//    any arithmetic, so the next item's MMAs start within a few hundred cycles.
 //  - The MMA and TMA warps issue from all 32 lanes through elect.sync; the
 //    forward's kernels use programmatic dependent launch.
 //  - For L1 a CTA's 128 weight rows are gate and up of 64 channels in bands
@@ -50,8 +58,9 @@ namespace moeffn {
 // warp roles: 0..11 drain TMEM (three warps per lane quarter, taking every
 // third 32-column chunk); 12 and 13 issue the MMAs of the even and the odd
 // tiles of the pair (leader; idle in the peer); 14 and 15 issue the TMA
-// copies of the two rings of stages (both CTAs; the copies of both signal
-// the leader's barrier of the stage).  The MMA and TMA
+// copies of the two rings of stages, or 14 alone those of the one paired
+// ring (both CTAs; the copies of both signal the leader's barrier of the
+// stage).  The MMA and TMA
 // warps issue from all 32 lanes through elect.sync: issued from one lane of a
 // divergent branch a block-scaled MMA costs about twice its tensor-pipe time.
 constexpr int kEpiWarps = 12;
