@@ -628,8 +628,16 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
 #pragma unroll
                         for (int i = 0; i < 16; ++i) h[i] = silu_fast(g[i]) * u[i] * __shfl_sync(0xffffffffu, wl, i);
                     } else {
+                        // two tokens at a time in packed FP32x2 arithmetic: the same roundings,
+                        // (silu(g) * u) * w, as the scalar form
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) h[i] = silu(g[i]) * u[i] * __shfl_sync(0xffffffffu, wl, i);
+                        for (int i = 0; i < 16; i += 2) {
+                            const float2 s = silu_x2(make_float2(g[i], g[i + 1]));
+                            const float2 wt = make_float2(__shfl_sync(0xffffffffu, wl, i), __shfl_sync(0xffffffffu, wl, i + 1));
+                            const float2 hv = __fmul2_rn(__fmul2_rn(s, make_float2(u[i], u[i + 1])), wt);
+                            h[i] = hv.x;
+                            h[i + 1] = hv.y;
+                        }
                     }
                     // Per token: amax over the 32 channels of the group (the warp's lanes).
                     // A halving exchange: after the shuffle across lane bit b, a lane keeps
@@ -660,8 +668,10 @@ grouped_gemm_kernel(const __grid_constant__ LayerMaps m1, const __grid_constant_
                     uint8_t* stg = reinterpret_cast<uint8_t*>(const_cast<__nv_bfloat16*>(take));
 #pragma unroll
                     for (int i = 0; i < 16; i += 2) {
-                        const uint32_t c2 = e4m3x2(h[i] * __shfl_sync(0xffffffffu, my_s, 2 * i),
-                                                   h[i + 1] * __shfl_sync(0xffffffffu, my_s, 2 * i + 2));
+                        const float2 sv = __fmul2_rn(make_float2(h[i], h[i + 1]),
+                                                     make_float2(__shfl_sync(0xffffffffu, my_s, 2 * i),
+                                                                 __shfl_sync(0xffffffffu, my_s, 2 * i + 2)));
+                        const uint32_t c2 = e4m3x2(sv.x, sv.y);
                         stg[i * 32 + lane] = static_cast<uint8_t>(c2);
                         stg[(i + 1) * 32 + lane] = static_cast<uint8_t>(c2 >> 8);
                     }

@@ -6,6 +6,8 @@
 //      [1, 2^128) or, for every 4096th pair, +inf; pairs with 0 < |a| < 2^-100
 //      or a subnormal quotient are not counted (they may differ in the last
 //      place).
+// The packed two-quotient form (div_by_ge1x2) is held to the same bars: in
+// both checks its halves must equal the scalar form.
 // Prints "mismatches <n1> <n2>" and exits 0 if the kernels ran.
 #include "common.cuh"
 
@@ -13,6 +15,7 @@
 #include <cstring>
 
 using moeffn::div_by_ge1;
+using moeffn::div_by_ge1x2;
 
 __device__ __forceinline__ bool same_bits(float x, float y) {
     return (isnan(x) && isnan(y)) || __float_as_uint(x) == __float_as_uint(y);
@@ -24,7 +27,11 @@ __global__ void check_bf16(unsigned int* bad, float* rec) {
     const float g = __uint_as_float(i << 16);
     const float b = 1.0f + expf(-g);
     const float q = div_by_ge1(g, b), r = g / b;
-    if (!same_bits(q, r)) {
+    // the packed form, this value in either half (the other half: the next BF16 value)
+    const float g2 = __uint_as_float(((i + 1u) & 0xFFFFu) << 16);
+    const float2 p = div_by_ge1x2(make_float2(g, g2), make_float2(b, 1.0f + expf(-g2)));
+    const float2 p2 = div_by_ge1x2(make_float2(g2, g), make_float2(1.0f + expf(-g2), b));
+    if (!same_bits(q, r) || !same_bits(p.x, r) || !same_bits(p2.y, r)) {
         const unsigned int k = atomicAdd(bad, 1u);
         if (k < 8) { rec[4 * k] = g; rec[4 * k + 1] = b; rec[4 * k + 2] = q; rec[4 * k + 3] = r; }
     }
@@ -44,10 +51,14 @@ __global__ void check_random(unsigned int n, unsigned int* bad, float* rec) {
     float b = __uint_as_float(((127u + rb % 128u) << 23) | (mix(rb) & 0x7FFFFFu));
     if ((i & 4095u) == 0) b = __uint_as_float(0x7F800000u);
     const float q = div_by_ge1(a, b), r = a / b;
+    // the packed form with this pair in either half must equal the scalar form everywhere
+    const float2 p1 = div_by_ge1x2(make_float2(a, 1.0f), make_float2(b, 3.0f));
+    const float2 p2 = div_by_ge1x2(make_float2(-1.0f, a), make_float2(2.0f, b));
+    const bool packed_ok = same_bits(p1.x, q) && same_bits(p2.y, q);
     // a dividend below 2^-100 in magnitude (or a subnormal quotient) may differ in
     // the last place; the exhaustive check above covers every BF16 input of SiLU
     const bool tiny = (a != 0.0f && fabsf(a) < 0x1p-100f) || (r != 0.0f && fabsf(r) < 0x1p-126f);
-    if (!tiny && !same_bits(q, r)) {
+    if ((!tiny && !same_bits(q, r)) || !packed_ok) {
         const unsigned int k = atomicAdd(bad, 1u);
         if (k < 8) { rec[4 * k] = a; rec[4 * k + 1] = b; rec[4 * k + 2] = q; rec[4 * k + 3] = r; }
     }
