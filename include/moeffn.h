@@ -117,8 +117,8 @@ typedef struct moeffn_problem {
 
 /* Views into a workspace after moeffn_forward (for inspection and tests).
  * P_max = align(T*min(k,E) + E*127, 128) pool rows; P = offsets[E] <= P_max
- * rows are in use; NT_max = ceil(T*k/tile_n) + E token tiles (+ 2E when
- * tiles are paired).  The n-th tile
+ * rows are in use; NT_max = ceil(T*k/tile_n) + E token tiles (+ 2E instead
+ * of + E when tiles are paired).  The n-th tile
  * of expert e has index tiles[e] + n and covers pool rows offsets[e] +
  * n*tile_rows[e] onwards.  Pool scale factors are stored per token tile and
  * per 128-wide K block as 256 uint32 words: word 128*h + 4*l + c holds the
