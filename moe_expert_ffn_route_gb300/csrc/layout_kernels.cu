@@ -26,6 +26,15 @@ namespace moeffn {
 // ---------------------------------------------------------------------------
 // a0: routing.  One warp per token; lane l holds logits l, l+32, ...
 // ---------------------------------------------------------------------------
+// Unsigned keys in the order of the floats they come from (no NaN, no -0).
+__device__ __forceinline__ uint32_t order_key(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float from_order_key(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 template <int PER_LANE>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
                                                          int E, int k, int64_t* __restrict__ idx,
@@ -40,9 +49,10 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     for (int i = 0; i < PER_LANE; ++i) {
         const int e = lane + 32 * i;
         // a NaN logit ranks below every number, like -inf: every candidate
-        // then compares, and each round picks a valid, untaken expert
+        // then compares, and each round picks a valid, untaken expert; -0 is
+        // taken as +0 (they compare equal, so ties between them go by index)
         const float x = e < E ? __ldg(l + e) : -INFINITY;
-        v[i] = x == x ? x : -INFINITY;
+        v[i] = x == x ? x + 0.0f : -INFINITY;
         if (e >= E) taken |= 1u << i;
     }
     float my_v = 0.f;
@@ -58,19 +68,13 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                 be = e;
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if (be < E && (be & 31) == lane) taken |= 1u << (be >> 5);
+        // across the warp: the largest value, then the lowest expert holding it
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, order_key(bv));
+        const int win = __reduce_min_sync(0xffffffffu, order_key(bv) == kmax ? be : 0x7FFFFFFF);
+        if (win < E && (win & 31) == lane) taken |= 1u << (win >> 5);
         if (lane == j) {
-            my_v = bv;
-            my_e = be;
+            my_v = from_order_key(kmax);
+            my_e = win;
         }
     }
     const float top = __shfl_sync(0xffffffffu, my_v, 0);

@@ -134,6 +134,23 @@ def test_route_nan_logits(E, k):
     np.testing.assert_allclose(gw[fin], rw[fin], rtol=2e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("E,k", [(40, 6), (256, 8), (1000, 8)])
+def test_route_ties_and_signed_zeros(E, k):
+    """Logits from a handful of values (many ties, +0 and -0 among them): the
+    ids equal the oracle's, which breaks ties by the lower expert index."""
+    rng = np.random.default_rng(E + 1)
+    levels = np.array([-1.0, -0.0, 0.0, 0.5, 0.5, 2.0], np.float32)
+    logits = levels[rng.integers(0, len(levels), size=(64, E))]
+    logits[5, :] = -0.0
+    logits[6, :] = 0.0
+    logits[6, ::2] = -0.0
+    ridx, rw = oracle.route(logits, k)
+    gidx, gw = mb.route_topk(up(logits), k)
+    torch.cuda.synchronize()
+    assert np.array_equal(gidx.cpu().numpy(), ridx)
+    np.testing.assert_allclose(gw.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
+
+
 @pytest.mark.parametrize("name", CONFIGS)
 def test_layout_parity(name):
     wl, inp, idx, w, run, _, _ = case(name)
