@@ -134,6 +134,25 @@ def test_route_nan_logits(E, k):
     np.testing.assert_allclose(gw[fin], rw[fin], rtol=2e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("name", ["medium", "prefill"])
+def test_forward_is_deterministic(name):
+    """A second forward on the same inputs, into a fresh workspace, gives the
+    same y (every token) and the same L1 codes and scales (the sampled tokens,
+    every token tile among them) bit for bit: no step sums in an order that
+    depends on timing."""
+    import copy
+    wl, inp, idx, w, run, tokens, _ = case(name)
+    run2 = copy.copy(run)
+    run2.ws = mb.empty_workspace(run.prob)
+    run2.y = mb.forward(run.prob, run.x, run.x_sf, run.idx, run.w, run.prepared, run2.ws)
+    torch.cuda.synchronize()
+    assert run2.status()[0] == mb.OK
+    assert torch.equal(run2.y.view(torch.int16), run.y.view(torch.int16))
+    c1, e1 = _l1_codes(run, run.tables(), tokens)
+    c2, e2 = _l1_codes(run2, run2.tables(), tokens)
+    assert np.array_equal(c1, c2) and np.array_equal(e1, e2)
+
+
 @pytest.mark.parametrize("E,k", [(40, 6), (256, 8), (1000, 8)])
 def test_route_ties_and_signed_zeros(E, k):
     """Logits from a handful of values (many ties, +0 and -0 among them): the
