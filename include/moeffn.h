@@ -56,7 +56,10 @@ typedef enum moeffn_status {
     MOEFFN_ERR_UNSUPPORTED = 2,          /* not an sm_103 device, or an option not built */
     MOEFFN_ERR_WORKSPACE_TOO_SMALL = 3,  /* a caller buffer is smaller than required */
     MOEFFN_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
-    MOEFFN_ERR_TIMEOUT = 5               /* a bounded device wait ran out (device status) */
+    MOEFFN_ERR_TIMEOUT = 5,              /* a bounded device wait ran out (device status) */
+    MOEFFN_ERR_OUT_OF_BOUNDS = 6         /* bounds-checked builds only (MOEFFN_BOUNDS_CHECK): a
+                                            device index outside its buffer was caught and the
+                                            access skipped (device status) */
 } moeffn_status;
 
 /* A cudaStream_t / CUstream handle passed through untouched. */

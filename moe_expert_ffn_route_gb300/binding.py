@@ -34,8 +34,9 @@ class Problem(ctypes.Structure):
 
 
 STATUS = {0: "MOEFFN_OK", 1: "MOEFFN_ERR_INVALID_ARG", 2: "MOEFFN_ERR_UNSUPPORTED",
-          3: "MOEFFN_ERR_WORKSPACE_TOO_SMALL", 4: "MOEFFN_ERR_CUDA", 5: "MOEFFN_ERR_TIMEOUT"}
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_TIMEOUT = range(6)
+          3: "MOEFFN_ERR_WORKSPACE_TOO_SMALL", 4: "MOEFFN_ERR_CUDA", 5: "MOEFFN_ERR_TIMEOUT",
+          6: "MOEFFN_ERR_OUT_OF_BOUNDS"}
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_TIMEOUT, ERR_OUT_OF_BOUNDS = range(7)
 DEBUG_STARVE_L1 = 1
 DEBUG_DUMP_L1_ACC = 2
 DEBUG_SPLIT_LAYERS = 4
@@ -89,12 +90,18 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         if not build_if_missing:
             raise FileNotFoundError(f"CUDA library not built: {path}")
         path = _build.build()
+    _lib = open_library(path)
+    return _lib
+
+
+def open_library(path: str) -> ctypes.CDLL:
+    """Open a build of the library (e.g. the bounds-checked variant) with the
+    entry points' signatures set; load() opens the product build."""
     L = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(L, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = L
     return L
 
 

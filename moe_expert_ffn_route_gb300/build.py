@@ -2,7 +2,9 @@
 
 Each translation unit is compiled by nvcc in parallel, then linked into one
 shared library under ``_build/<machine>/``.  A stamp of the sources and
-flags skips rebuilds when nothing changed.
+flags skips rebuilds when nothing changed.  ``variant="bounds"`` builds
+libmoeffn_bounds.so with MOEFFN_BOUNDS_CHECK (device index checks that report
+through the status word; for tests).
 """
 from __future__ import annotations
 
@@ -29,33 +31,38 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else (shutil.which("nvcc") or "nvcc")
 
 
-def lib_path() -> str:
-    return os.path.join(HERE, "_build", platform.machine(), "libmoeffn.so")
+VARIANTS = {"": [], "bounds": ["-DMOEFFN_BOUNDS_CHECK"]}
 
 
-def _digest() -> str:
+def lib_path(variant: str = "") -> str:
+    name = "libmoeffn.so" if not variant else f"libmoeffn_{variant}.so"
+    return os.path.join(HERE, "_build", platform.machine(), name)
+
+
+def _digest(flags) -> str:
     h = hashlib.sha256()
     for f in SOURCES + HEADERS:
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(fh.read())
     with open(os.path.join(INCLUDE, "moeffn.h"), "rb") as fh:
         h.update(fh.read())
-    h.update(" ".join(ARCH + FLAGS).encode())
+    h.update(" ".join(ARCH + flags).encode())
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    so = lib_path()
-    out = os.path.dirname(so)
+def build(force: bool = False, verbose: bool = False, variant: str = "") -> str:
+    so = lib_path(variant)
+    flags = FLAGS + VARIANTS[variant]
+    out = os.path.join(os.path.dirname(so), variant or "product")
     os.makedirs(out, exist_ok=True)
-    digest = _digest()
+    digest = _digest(flags)
     stamp = so + ".stamp"
     if not force and os.path.exists(so) and os.path.exists(stamp) and open(stamp).read().strip() == digest:
         return so
 
     def compile_one(src: str) -> str:
         obj = os.path.join(out, src.replace(".cu", ".o"))
-        cmd = [nvcc()] + ARCH + FLAGS + ["-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc()] + ARCH + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -204,6 +204,7 @@ const char* moeffn_status_string(moeffn_status s) {
         case MOEFFN_ERR_WORKSPACE_TOO_SMALL: return "buffer too small";
         case MOEFFN_ERR_CUDA: return "CUDA error";
         case MOEFFN_ERR_TIMEOUT: return "device wait timed out";
+        case MOEFFN_ERR_OUT_OF_BOUNDS: return "device index out of bounds";
     }
     return "unknown status";
 }
@@ -322,7 +323,7 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
                   reinterpret_cast<int*>(w + L.hist), reinterpret_cast<int*>(w + L.rank), counts, offsets,
                   tiles, tile_rows, tile_rec, l1_done, slots, reinterpret_cast<int*>(w + L.row2tk), reinterpret_cast<float*>(w + L.wpool),
                   reinterpret_cast<int*>(w + L.slack), w + L.xpool, reinterpret_cast<uint32_t*>(w + L.xpool_sf),
-                  status};
+                  status, static_cast<int>(L.P_max), static_cast<int>(L.NT_max)};
     if (launch_layout(la, st) != cudaSuccess || !mark(1)) return MOEFFN_ERR_CUDA;
 
     const PrepLayout PL = prep_layout(*p);
@@ -384,7 +385,8 @@ moeffn_status forward_impl(const moeffn_problem* p, const uint8_t* x, const uint
         if (launch_gemm(m1, m2, g, st) != cudaSuccess || !mark(2) || !mark(3)) return MOEFFN_ERR_CUDA;
     }
 
-    if (launch_combine(reinterpret_cast<const uint16_t*>(w + L.ypool), slots, T, H, k, y, st) != cudaSuccess ||
+    if (launch_combine(reinterpret_cast<const uint16_t*>(w + L.ypool), slots, T, H, k, y, static_cast<int>(L.P_max),
+                       status, st) != cudaSuccess ||
         !mark(4))
         return MOEFFN_ERR_CUDA;
     return MOEFFN_OK;
@@ -455,6 +457,7 @@ moeffn_status moeffn_get_device_status(const moeffn_problem* p, void* workspace,
         detail[0] = words[0];
         detail[1] = words[1];
     }
+    if (words[0] & DEV_ERR_BOUNDS) return MOEFFN_ERR_OUT_OF_BOUNDS;
     if (words[0] & DEV_ERR_TIMEOUT) return MOEFFN_ERR_TIMEOUT;
     if (words[0] & DEV_ERR_BAD_EXPERT) return MOEFFN_ERR_INVALID_ARG;
     return MOEFFN_OK;

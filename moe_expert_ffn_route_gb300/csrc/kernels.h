@@ -39,6 +39,7 @@ struct LayoutArgs {
     uint8_t* xpool;       // [P_max][H]
     uint32_t* xpool_sf;   // [NT_max][H/128][2][128]
     DevStatus* status;
+    int P_max, NT_max;    // pool rows and token tiles the workspace holds (bounds-checked builds)
 };
 
 struct PrepareArgs {
@@ -80,7 +81,7 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int64_t*
                               cudaStream_t stream);
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const uint16_t* ypool, const int* slots, int T, int H, int k,
-                           uint16_t* y, cudaStream_t stream);
+                           uint16_t* y, int P_max, DevStatus* status, cudaStream_t stream);
 cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t stream);
 // Tensor maps of one grouped GEMM launch: the prepared weights (boxes of
 // 128 rows x 128 K), the token pool (boxes of 8, 16, ..., kMaxTileN/2 rows,

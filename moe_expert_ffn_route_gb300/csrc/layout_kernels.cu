@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
     const int* __restrict__ tiles, const int* __restrict__ tile_rows, int* __restrict__ tile_rec,
     int* __restrict__ l1_done, int* __restrict__ slots, int* __restrict__ row2tk,
     float* __restrict__ wpool, int* __restrict__ slack, uint8_t* __restrict__ xpool,
-    uint32_t* __restrict__ xpool_sf, int nb_tok) {
+    uint32_t* __restrict__ xpool_sf, int nb_tok, int P_max, int NT_max, DevStatus* st) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_wait();
     pdl_launch_dependents();
@@ -248,17 +248,25 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
         const int e = blockIdx.x - nb_tok;
         const int n = counts[e], beg = offsets[e], end = offsets[e + 1];
         const int t0 = tiles[e], t1 = tiles[e + 1];
+        // the GEMM's pool rows and tile indices come from these records: its rows
+        // lie in [beg, beg + n) and its tiles in [t0, t1), checked here once
+        if (threadIdx.x == 0 && (!in_bounds(st, end - 1, P_max, 1) || !in_bounds(st, beg + n - 1, end, 1) ||
+                                 !in_bounds(st, t1 - 1, NT_max, 2)))
+            return;
         for (int tt = t0 + threadIdx.x; tt < t1; tt += blockDim.x) {
+            if (!in_bounds(st, tt, NT_max, 2)) break;
             int4* rec = reinterpret_cast<int4*>(tile_rec) + 2 * tt;
             rec[0] = make_int4(e, t0, t1 - t0, tile_rows[e]);
             rec[1] = make_int4(beg, n, 0, 0);
             l1_done[tt] = 0;    // counts the L1 epilogue warps that published this tile's rows
         }
         for (int r = beg + n + threadIdx.x; r < end; r += blockDim.x) {
+            if (!in_bounds(st, r, P_max, 3)) break;
             row2tk[r] = -1;
             wpool[r] = 0.f;
         }
         for (int b = beg / kPoolBlock + threadIdx.x; b < end / kPoolBlock; b += blockDim.x) {
+            if (!in_bounds(st, b, P_max / kPoolBlock, 4)) break;
             const int real = min(kPoolBlock, max(0, n - (b * kPoolBlock - beg)));
             slack[b] = kPoolBlock - real;
         }
@@ -281,10 +289,11 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
             slot = offsets[e] + r;
             const int rows = tile_rows[e];
             chunk = tiles[e] + r / rows;
+            if (!in_bounds(st, slot, P_max, 5) || !in_bounds(st, chunk, NT_max, 6)) slot = chunk = -1;
             const int rt = r % rows;
             // 128-row half of the tile, then word 4 l + c for row 32 c + l of that half
             word = (rt >> 7) * 128 + (rt & 31) * 4 + ((rt & 127) >> 5);
-            if (part == 0) {
+            if (part == 0 && slot >= 0) {
                 row2tk[slot] = i;
                 wpool[slot] = topk_w[i];
             }
@@ -341,7 +350,8 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
     const int nb_tok = (a.T + tok_per_block - 1) / tok_per_block;
     return launch_pdl(dispatch_kernel, dim3(nb_tok + a.E), dim3(256), 0, stream, a.x, a.x_sf, a.topk_idx,
                       a.topk_w, a.T, a.H, a.E, a.k, a.hist, a.rank, a.counts, a.offsets, a.tiles, a.tile_rows,
-                      a.tile_rec, a.l1_done, a.slots, a.row2tk, a.wpool, a.slack, a.xpool, a.xpool_sf, nb_tok);
+                      a.tile_rec, a.l1_done, a.slots, a.row2tk, a.wpool, a.slack, a.xpool, a.xpool_sf, nb_tok,
+                      a.P_max, a.NT_max, a.status);
 }
 
 // ---------------------------------------------------------------------------
@@ -350,12 +360,15 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t stream) {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ ypool,
                                                       const int* __restrict__ slots, int H, int k,
-                                                      uint16_t* __restrict__ y) {
+                                                      uint16_t* __restrict__ y, int P_max, DevStatus* st) {
     __shared__ int s_slot[32];
     const int t = blockIdx.x;
     pdl_wait();
     pdl_launch_dependents();
-    if (threadIdx.x < k) s_slot[threadIdx.x] = slots[static_cast<size_t>(t) * k + threadIdx.x];
+    if (threadIdx.x < k) {
+        const int s = slots[static_cast<size_t>(t) * k + threadIdx.x];
+        s_slot[threadIdx.x] = s < 0 || in_bounds(st, s, P_max, 7) ? s : -1;
+    }
     __syncthreads();
     const int nv = H / 8;
     for (int v = threadIdx.x; v < nv; v += blockDim.x) {
@@ -393,9 +406,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
 }
 
 cudaError_t launch_combine(const uint16_t* ypool, const int* slots, int T, int H, int k,
-                           uint16_t* y, cudaStream_t stream) {
+                           uint16_t* y, int P_max, DevStatus* status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    return launch_pdl(combine_kernel, dim3(T), dim3(128), 0, stream, ypool, slots, H, k, y);
+    return launch_pdl(combine_kernel, dim3(T), dim3(128), 0, stream, ypool, slots, H, k, y, P_max, status);
 }
 
 // ---------------------------------------------------------------------------

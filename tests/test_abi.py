@@ -29,8 +29,8 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for s in range(6):
-        assert mb.status_string(s)
+    for s in range(7):
+        assert mb.status_string(s) != "unknown status"
     assert mb.status_string(99) == "unknown status"
 
 
