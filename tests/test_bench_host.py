@@ -70,9 +70,9 @@ def test_roofline_peaks():
 def test_traffic_lookup_follows_the_kernel_hash():
     text = open(os.path.join(ROOT, "profiles", "grouped_gemm_traffic.md")).read()
     recorded = text.split("kernel source sha256:")[1].split()[0]
-    assert bench.traffic_from_profile(recorded, "prefill", 1.0) == 7551840255.0
-    assert bench.traffic_from_profile(recorded, "prefill", 2.0) == 2 * 7551840255.0
-    assert bench.traffic_from_profile(recorded, "decode", 1.0) == 6009696687.0
+    assert bench.traffic_from_profile(recorded, "prefill", 1.0) == 7550064640.0
+    assert bench.traffic_from_profile(recorded, "prefill", 2.0) == 2 * 7550064640.0
+    assert bench.traffic_from_profile(recorded, "decode", 1.0) == 6010465480.0
     assert bench.traffic_from_profile("0" * 64, "prefill", 1.0) is None     # another kernel source
     assert bench.traffic_from_profile(recorded, "no-such-workload", 1.0) is None
 
