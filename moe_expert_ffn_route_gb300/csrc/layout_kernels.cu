@@ -249,10 +249,10 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
         const int n = counts[e], beg = offsets[e], end = offsets[e + 1];
         const int t0 = tiles[e], t1 = tiles[e + 1];
         // the GEMM's pool rows and tile indices come from these records: its rows
-        // lie in [beg, beg + n) and its tiles in [t0, t1), checked here once
-        if (threadIdx.x == 0 && (!in_bounds(st, end - 1, P_max, 1) || !in_bounds(st, beg + n - 1, end, 1) ||
-                                 !in_bounds(st, t1 - 1, NT_max, 2)))
-            return;
+        // lie in [beg, beg + n) within [beg, end), its tiles in [t0, t1); the
+        // block checks the non-empty ranges here, all threads alike
+        if (end > beg && (!in_bounds(st, end - 1, P_max, 1) || !in_bounds(st, beg + n, end + 1, 1))) return;
+        if (t1 > t0 && !in_bounds(st, t1 - 1, NT_max, 2)) return;
         for (int tt = t0 + threadIdx.x; tt < t1; tt += blockDim.x) {
             if (!in_bounds(st, tt, NT_max, 2)) break;
             int4* rec = reinterpret_cast<int4*>(tile_rec) + 2 * tt;

@@ -39,12 +39,14 @@ def bounds_library():
     mb._lib = saved
 
 
-def _routed(T, H, I, E, k, seed, empty=0.0, skew=False):
+def _routed(T, H, I, E, k, seed, empty=0.0, skew=False, first_empty=False):
     inp = synth.make_inputs(synth.Workload(f"bounds{seed}", T, H, I, E, k, seed))
     logits = inp["logits"].copy()
     if skew:
         logits[:, 0] += 5.0
         logits[:, E - 1] -= 50.0
+    if first_empty:
+        logits[:, 0] -= 50.0                    # expert 0 gets no rows (empty first segment)
     idx, w = oracle.route(logits, k)
     if empty:
         idx = idx.copy()
@@ -54,7 +56,7 @@ def _routed(T, H, I, E, k, seed, empty=0.0, skew=False):
 
 # (T, H, I, E, k, tile_n, extra): 32-row tiles; paired 48-row tiles with a
 # skewed expert; one-tile-per-stage 144; 224; empty entries; H = 384 (an L2
-# tail half, paired); one expert
+# tail half, paired); one expert; expert 0 without rows, paired
 CASES = [
     (96, 512, 256, 6, 2, 0, {}),
     (200, 512, 256, 5, 2, 48, {"skew": True}),
@@ -63,6 +65,7 @@ CASES = [
     (37, 512, 256, 7, 3, 0, {"empty": 0.3}),
     (300, 384, 128, 3, 2, 0, {}),
     (200, 512, 256, 1, 1, 0, {}),
+    (300, 512, 256, 5, 2, 48, {"first_empty": True}),
 ]
 
 
